@@ -1,0 +1,184 @@
+"""The oracle: a plain, slow fp64 CPU implementation of C = A . deq(B)^T.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s ``cpu_baseline`` / ``--impl reference`` leg may import this
+package.  The product library under ``weight_only_bit_w4a16_gb300/`` never
+imports it, and the two share no code, header, table or constant.
+
+The arithmetic lives in ``wq_oracle.c`` (plain C, fp64, bit-by-bit decoders,
+an explicit e2m1 table, a plain k-ascending dot product).  This module only
+builds that file with gcc, loads it with ctypes and marshals numpy arrays.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against values
+fixed by the pages and by the mathematics (hand-worked bytes, exhaustive
+decodes against independent decoders, exact rational dot products, exact
+invariants); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "wq_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD_DIR, "libwq_oracle.so")
+
+#: format codes of the oracle's own C interface
+FORMATS = {"nvfp4": 0, "mxfp4": 1, "int4": 2}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile wq_oracle.c into a shared library (gcc, fp64, no FMA contraction)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_SO)
+            and os.path.getmtime(_SO) >= os.path.getmtime(_SRC)):
+        return _SO
+    tmp = _SO + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-std=c99", "-Wall", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_SO)
+            d, i, vp = ctypes.c_double, ctypes.c_int, ctypes.c_void_p
+            L.wqo_e2m1.restype = d; L.wqo_e2m1.argtypes = [i]
+            L.wqo_e4m3.restype = d; L.wqo_e4m3.argtypes = [i]
+            L.wqo_e8m0.restype = d; L.wqo_e8m0.argtypes = [i]
+            L.wqo_bf16.restype = d; L.wqo_bf16.argtypes = [i]
+            L.wqo_round_bf16.restype = i; L.wqo_round_bf16.argtypes = [d]
+            L.wqo_weight.restype = d
+            L.wqo_weight.argtypes = [vp, vp, vp, i, i, i, i, i, i]
+            L.wqo_dequant.restype = None
+            L.wqo_dequant.argtypes = [vp, vp, vp, i, i, i, i, vp, vp]
+            L.wqo_gemm.restype = None
+            L.wqo_gemm.argtypes = [vp, vp, vp, vp, i, i, i, i, i,
+                                   vp, i, vp, i, vp, vp]
+            L.wqo_max_threads.restype = i; L.wqo_max_threads.argtypes = []
+            L.wqo_set_threads.restype = None; L.wqo_set_threads.argtypes = [i]
+            _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _fmt(fmt) -> int:
+    return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+# -- scalar decoders (exposed for the pins) ----------------------------------
+def e2m1(code: int) -> float:
+    return lib().wqo_e2m1(int(code))
+
+
+def e4m3(byte: int) -> float:
+    return lib().wqo_e4m3(int(byte))
+
+
+def e8m0(byte: int) -> float:
+    return lib().wqo_e8m0(int(byte))
+
+
+def bf16(bits: int) -> float:
+    return lib().wqo_bf16(int(bits))
+
+
+def round_bf16(x: float) -> int:
+    """bf16 bits of x rounded to nearest even (uint16 value)."""
+    return lib().wqo_round_bf16(float(x)) & 0xFFFF
+
+
+# -- array entry points -------------------------------------------------------
+def _check(packed, scales, zeros, fmt, group):
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    N, Kh = packed.shape
+    K = 2 * Kh
+    f = _fmt(fmt)
+    sdt = np.uint16 if f == FORMATS["int4"] else np.uint8
+    scales = np.ascontiguousarray(scales, dtype=sdt)
+    assert scales.shape == (N, K // group), (scales.shape, N, K, group)
+    if f == FORMATS["int4"]:
+        zeros = np.ascontiguousarray(zeros, dtype=np.uint8)
+        assert zeros.shape == (N, K // group)
+    else:
+        zeros = None
+    return packed, scales, zeros, N, K, f
+
+
+def weight(packed, scales, zeros, fmt, group, n, k) -> float:
+    packed, scales, zeros, N, K, f = _check(packed, scales, zeros, fmt, group)
+    return lib().wqo_weight(_ptr(packed), _ptr(scales), _ptr(zeros), N, K, f,
+                            int(group), int(n), int(k))
+
+
+def dequant(packed, scales, zeros, fmt, group):
+    """Return (W64, Wbf16): exact fp64 weights and their RNE bf16 bits, (N, K)."""
+    packed, scales, zeros, N, K, f = _check(packed, scales, zeros, fmt, group)
+    W64 = np.empty((N, K), dtype=np.float64)
+    Wb = np.empty((N, K), dtype=np.uint16)
+    lib().wqo_dequant(_ptr(packed), _ptr(scales), _ptr(zeros), N, K, f,
+                      int(group), _ptr(W64), _ptr(Wb))
+    return W64, Wb
+
+
+def gemm(A_bits, packed, scales, zeros, fmt, group, rows=None, cols=None):
+    """Return (C, S): the exact fp64 product and the tolerance scale.
+
+    A_bits is the (M, K) bf16 activation as uint16 bits.  ``rows`` / ``cols``
+    select a subset of output rows (m) / columns (n); None means all.
+    """
+    packed, scales, zeros, N, K, f = _check(packed, scales, zeros, fmt, group)
+    A_bits = np.ascontiguousarray(A_bits, dtype=np.uint16)
+    M = A_bits.shape[0]
+    assert A_bits.shape == (M, K)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    c = None if cols is None else np.ascontiguousarray(cols, dtype=np.int32)
+    nr = M if r is None else len(r)
+    nc = N if c is None else len(c)
+    if r is not None:
+        assert r.size == 0 or (r.min() >= 0 and r.max() < M)
+    if c is not None:
+        assert c.size == 0 or (c.min() >= 0 and c.max() < N)
+    C = np.zeros((nr, nc), dtype=np.float64)
+    S = np.zeros((nr, nc), dtype=np.float64)
+    if nr and nc and K:
+        lib().wqo_gemm(_ptr(A_bits), _ptr(packed), _ptr(scales), _ptr(zeros),
+                       M, N, K, f, int(group), _ptr(r), nr, _ptr(c), nc,
+                       _ptr(C), _ptr(S))
+    return C, S
+
+
+def tolerance(C_exact, S, out_dtype: str):
+    """Allowed |C_gpu - C_exact| per element.
+
+    fp32 output: 1e-3 * S + 1e-6; bf16 output adds 2^-8 * |C_exact| for the
+    final rounding of the output.
+    """
+    tol = 1e-3 * np.asarray(S) + 1e-6
+    if out_dtype == "bf16":
+        tol = tol + np.abs(np.asarray(C_exact)) * 2.0 ** -8
+    return tol
+
+
+def max_threads() -> int:
+    return lib().wqo_max_threads()
+
+
+def set_threads(n: int) -> None:
+    lib().wqo_set_threads(int(n))

@@ -1,0 +1,532 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 W4A16 dequantise-GEMM library.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode_int4|prefill_mxfp4|large_nvfp4|tiny_nvfp4]
+
+Default workload (decode_int4): the decode GEMV of the 3B int4-g128 model's
+gate/up projection, N=8192, K=3072, bf16 activations, bf16 output.  One STEP
+is the whole hot path over one batch: three wq_gemm calls, at M = 1, 4 and
+16, each on its own weight set.  R distinct device copies of the weights
+(more than twice the L2 size in total) are rotated, so every call streams its
+weights from HBM.  The timed steps are replayed from CUDA graphs, K steps
+exactly, bracketed by a barrier and cudaDeviceSynchronize, timed with CUDA
+events on the launching stream, max over ranks.  The metric is the effective
+weight bandwidth (packed codes + scales + zeros per call / time).
+
+Prints ONE JSON line on rank 0 (keys described in the design notes):
+metric, value, unit, roofline (dominant kernel, live CUDA-event timing),
+cpu_baseline (the oracle on the host cores, bounded sample), e2e (through the
+public Python API with pinned host buffers), clocks (nvidia-smi sampled
+during the timed region), gpu_launches.
+
+--impl reference times the oracle (the fp64 CPU implementation under
+oracle/) on the same workload and prints the same line with
+"impl": "reference".  Under torchrun every rank runs an independent replica
+(the path has no exchange step); value is the aggregate over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+BENCH_WORKLOADS = {
+    "decode_int4": dict(fmt="int4", group=128, Ms=(1, 4, 16), N=8192, K=3072, out="bf16",
+                        bound="hbm", metric="weight HBM GB/s (M≤16)", unit="GB/s"),
+    "prefill_mxfp4": dict(fmt="mxfp4", group=32, Ms=(2048,), N=3072, K=3072, out="bf16",
+                          bound="tensor", metric="dequant-GEMM TFLOP/s (large M)", unit="TFLOP/s"),
+    "large_nvfp4": dict(fmt="nvfp4", group=16, Ms=(8192,), N=8192, K=8192, out="bf16", scale_mult=1.0,
+                        bound="tensor", metric="dequant-GEMM TFLOP/s (large M)", unit="TFLOP/s"),
+    "tiny_nvfp4": dict(fmt="nvfp4", group=16, Ms=(16,), N=256, K=512, out="fp32",
+                       bound="hbm", metric="weight HBM GB/s (M≤16)", unit="GB/s"),
+}
+
+KERNEL_SOURCES = {  # files whose content defines the dominant kernel of a workload
+    "decode_int4": ["wq_gemv.cu", "wq_common.cuh"],
+    "tiny_nvfp4": ["wq_gemv.cu", "wq_common.cuh"],
+    "prefill_mxfp4": ["wq_tc.cu", "wq_tc.cuh", "wq_common.cuh"],
+    "large_nvfp4": ["wq_tc.cu", "wq_tc.cuh", "wq_common.cuh"],
+}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas; timing max over ranks)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(use_cuda: bool):
+    ws, rank, _ = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend="nccl" if use_cuda else "gloo")
+    return ws, rank
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str, period_ms: int = 50):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms={period_ms}", "-i", gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, smax = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            reasons = [r for r, v in zip(self.REASONS, parts[5:9]) if v.lower() == "active"]
+            self.samples.append((time.monotonic(), sm, smax, reasons))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return None
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed"
+        if not inside:   # timed region shorter than the sampling period: nearest samples
+            inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            window = "nearest to timed region"
+        sm = sorted(s[1] for s in inside)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": sorted({r for s in inside for r in s[3]}), "samples": len(inside),
+                "window": window}
+
+
+# ---------------------------------------------------------------------------
+# roofline helpers
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_hash(workload: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[workload]:
+        p = os.path.join(ROOT, "weight_only_bit_w4a16_gb300", "csrc", f)
+        if os.path.exists(p):
+            with open(p, "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (profiles/traffic.txt: workload hash bytes)."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    want = kernel_hash(workload)
+    with open(p) as f:
+        for line in f:
+            parts = line.split("#")[0].split()
+            if len(parts) >= 3 and parts[0] == workload and parts[1] == want:
+                return float(parts[2])
+    return None
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores
+# ---------------------------------------------------------------------------
+def oracle_step_sample(w, cols_per_call: int, A_by_M, weights, seed=0):
+    """Run the oracle on a column sample of every call of one step; returns
+    (seconds, weight bytes covered)."""
+    import oracle
+    from weight_only_bit_w4a16_gb300 import metrics
+    packed, scales, zeros = weights
+    rng = np.random.default_rng(seed)
+    t = time.perf_counter()
+    covered = 0
+    for M in w["Ms"]:
+        cols = np.sort(rng.choice(w["N"], size=cols_per_call, replace=False))
+        oracle.gemm(A_by_M[M], packed, scales, zeros, w["fmt"], w["group"], cols=cols)
+        covered += metrics.weight_bytes(w["fmt"], cols_per_call, w["K"], w["group"])
+    return time.perf_counter() - t, covered
+
+
+def oracle_rate(w, A_by_M, weights, budget_s: float):
+    """Calibrate a column sample to about budget_s of oracle work per step."""
+    cols = min(w["N"], 64)
+    dt, _ = oracle_step_sample(w, cols, A_by_M, weights)
+    cols = int(max(1, min(w["N"], cols * budget_s / max(dt, 1e-6))))
+    return cols
+
+
+def host_inputs(w, seed=0):
+    from weight_only_bit_w4a16_gb300 import synth
+    weights = synth.make_weights(w["fmt"], w["N"], w["K"], w["group"], seed=seed,
+                                 scale_mult=w.get("scale_mult", 0.5))
+    A_by_M = {M: synth.draw_A(np.random.default_rng(seed + 1000 + M), M, w["K"]) for M in w["Ms"]}
+    return A_by_M, weights
+
+
+def cpu_baseline(w, A_by_M, weights, budget_s=15.0):
+    import oracle
+    cols = oracle_rate(w, A_by_M, weights, budget_s)
+    dt, covered = oracle_step_sample(w, cols, A_by_M, weights, seed=1)
+    from weight_only_bit_w4a16_gb300 import metrics
+    flops = sum(metrics.call_flops(M, cols, w["K"]) for M in w["Ms"])
+    value = covered / dt / 1e9 if w["unit"] == "GB/s" else flops / dt / 1e12
+    return {"value": value, "unit": w["unit"], "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{cols} of {w['N']} output columns of each call of one step "
+                      f"(M={list(w['Ms'])}, K={w['K']}), {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import weight_only_bit_w4a16_gb300 as wq
+    from weight_only_bit_w4a16_gb300 import metrics
+
+    ws, rank = dist_init(use_cuda=True)
+    _, _, local = dist_env()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    wq.lib()   # fails loudly without the built library
+    w = BENCH_WORKLOADS[args.workload]
+    fmt, group, Ms, N, K, out = w["fmt"], w["group"], w["Ms"], w["N"], w["K"], w["out"]
+    fcode = wq.FORMATS[fmt] | (wq.WQ_OUT_F32 if out == "fp32" else 0)
+    odt = torch.float32 if out == "fp32" else torch.bfloat16
+
+    A_by_M, weights = host_inputs(w)
+    packed_h, scales_h, zeros_h = weights
+    wb = metrics.weight_bytes(fmt, N, K, group)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 * 1024 * 1024)
+    per_step_w = wb * len(Ms)
+    R = max(2 * len(Ms), math.ceil(2.0 * l2 / wb))
+    R = int(math.ceil(R / len(Ms)) * len(Ms))
+
+    def up(a):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    packed0 = up(packed_h)
+    scales0 = up(scales_h.view(np.int16) if fmt == "int4" else scales_h)
+    zeros0 = up(zeros_h)
+    pool = [(packed0.clone(), scales0.clone(), None if zeros0 is None else zeros0.clone()) for _ in range(R)]
+    del packed0, scales0, zeros0
+    A_d = {M: up(A_by_M[M].view(np.int16)) for M in Ms}
+    C_d = {M: torch.empty((M, N), dtype=odt, device=dev) for M in Ms}
+    s = torch.cuda.Stream(dev)
+
+    def call(M, slot, stream_handle):
+        pk, sc, zr = pool[slot]
+        st = wq.wq_gemm_ex(A_d[M].data_ptr(), pk.data_ptr(), sc.data_ptr(),
+                           None if zr is None else zr.data_ptr(), C_d[M].data_ptr(), M, N, K, fcode, group,
+                           stream_handle, wq.WQ_PATH_AUTO)
+        if st != wq.WQ_OK:
+            raise wq.WQError(st, "wq_gemm_ex")
+
+    def capture(nsteps, Ms_used):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                h = torch.cuda.current_stream().cuda_stream
+                for i in range(nsteps):
+                    for j, M in enumerate(Ms_used):
+                        call(M, (i * len(Ms_used) + j) % R, h)
+        return g
+
+    # graphs of G steps; G * len(Ms) is a multiple of R so replays rotate seamlessly
+    G = R // len(Ms)
+    G *= max(1, math.ceil(64 / G))
+    with torch.cuda.stream(s):
+        for i in range(2):   # eager warm-up outside capture (module load, attributes)
+            for j, M in enumerate(Ms):
+                call(M, j, s.cuda_stream)
+    torch.cuda.synchronize()
+    g_full = capture(G, Ms)
+    rem = args.steps % G
+    g_rem = capture(rem, Ms) if rem else None
+
+    # warm-up (untimed): at least W steps
+    for _ in range(max(1, math.ceil(args.warmup / G))):
+        g_full.replay()
+    torch.cuda.synchronize()
+
+    gpu_id = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else str(local)
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    with torch.cuda.stream(s):
+        ev0.record(s)
+        for _ in range(args.steps // G):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(s)
+    torch.cuda.synchronize()
+    t1 = time.monotonic()
+    barrier()
+    time.sleep(0.15)
+    sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, dev)
+    launches = args.steps * len(Ms)
+    clocks = sampler.summary(t0, t1)
+
+    peaks = measured_peaks()
+    avg_launch_s = ms / 1e3 / launches
+    if w["bound"] == "hbm":
+        value = ws * args.steps * per_step_w / (ms_max / 1e3) / 1e9
+        algo = sum(metrics.call_bytes(fmt, M, N, K, group, out) for M in Ms) / len(Ms)
+        achieved = algo / avg_launch_s / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
+                "algorithmic_bytes_per_launch": algo, "peak_source": peaks["source"] + " hbm_gbs"}
+    else:
+        flops = sum(metrics.call_flops(M, N, K) for M in Ms)
+        value = ws * args.steps * flops / (ms_max / 1e3) / 1e12
+        algo = flops / len(Ms)
+        achieved = algo / avg_launch_s / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
+                "algorithmic_flops_per_launch": algo, "peak_source": peaks["source"] + " bf16_tflops (burst)"}
+
+    # per-M launch time (separate graphs of one M; not part of the timed steps)
+    per_m = {}
+    if w["bound"] == "hbm" and len(Ms) > 1:
+        for M in Ms:
+            gm = capture(R, (M,))
+            gm.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = max(1, 2000 // R)
+            with torch.cuda.stream(s):
+                e0.record(s)
+                for _ in range(reps):
+                    gm.replay()
+                e1.record(s)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (reps * R)
+            cb = metrics.call_bytes(fmt, M, N, K, group, out)
+            per_m[str(M)] = {"us_per_call": us, "weight_GBps": wb / us / 1e3,
+                             "roofline_frac": cb / us / 1e3 / peaks["hbm_gbs"]}
+
+    e2e = run_e2e(args, w, A_by_M, weights, pool, dev, ws)
+
+    result = {
+        "metric": w["metric"], "value": value, "unit": w["unit"], "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "format": fmt, "group": group, "M": list(Ms), "N": N, "K": K,
+                   "out": out, "calls_per_step": len(Ms),
+                   "l2": f"inputs larger than L2: {R} weight sets of {wb / 1e6:.2f} MB rotated "
+                         f"({R * wb / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
+                   "timing": "CUDA graphs of the timed steps, CUDA events on the launching stream",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": roof, "clocks": clocks, "gpu_launches": launches, "e2e": e2e,
+    }
+    if per_m:
+        result["per_m"] = per_m
+    if rank == 0 and ws == 1:
+        result["cpu_baseline"] = cpu_baseline(w, A_by_M, weights, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def run_e2e(args, w, A_by_M, weights, pool, dev, ws):
+    """The same metric through the public API (weight_only_bit_w4a16_gb300.gemm)
+    from pinned host memory.  Per step: H2D of each call's activations,
+    the calls on device-resident weights (uploaded once, as a model's weights
+    are), D2H of each result.  A second figure also uploads the weights every
+    step."""
+    import torch
+    import weight_only_bit_w4a16_gb300 as wq
+    from weight_only_bit_w4a16_gb300 import metrics
+    fmt, group, Ms, N, K, out = w["fmt"], w["group"], w["Ms"], w["N"], w["K"], w["out"]
+    odt = torch.float32 if out == "fp32" else torch.bfloat16
+    A_h = {M: torch.from_numpy(A_by_M[M].view(np.int16)).view(torch.bfloat16).pin_memory() for M in Ms}
+    C_h = {M: torch.empty((M, N), dtype=odt).pin_memory() for M in Ms}
+    A_d = {M: torch.empty((M, K), dtype=torch.bfloat16, device=dev) for M in Ms}
+    C_d = {M: torch.empty((M, N), dtype=odt, device=dev) for M in Ms}
+    s = torch.cuda.Stream(dev)
+    R = len(pool)
+    steps = max(1, min(args.steps, 2000))
+
+    def one(i, upload_weights=None):
+        for j, M in enumerate(Ms):
+            pk, sc, zr = pool[(i * len(Ms) + j) % R]
+            if upload_weights is not None:
+                pk.copy_(upload_weights[0], non_blocking=True)
+                sc.copy_(upload_weights[1], non_blocking=True)
+                if zr is not None:
+                    zr.copy_(upload_weights[2], non_blocking=True)
+            A_d[M].copy_(A_h[M], non_blocking=True)
+            wq.gemm(A_d[M], pk, sc, zr, fmt, group, out_dtype=out, out=C_d[M])
+            C_h[M].copy_(C_d[M], non_blocking=True)
+
+    def timed(nsteps, upload=None):
+        with torch.cuda.stream(s):
+            for i in range(3):
+                one(i, upload)
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for i in range(nsteps):
+                one(i, upload)
+            e1.record(s)
+        torch.cuda.synchronize()
+        return max_over_ranks(e0.elapsed_time(e1), dev)
+
+    h2d = sum(A_h[M].numel() * 2 for M in Ms)
+    d2h = sum(C_h[M].numel() * C_h[M].element_size() for M in Ms)
+    ms = timed(steps)
+    wbytes = metrics.weight_bytes(fmt, N, K, group)
+    if w["unit"] == "GB/s":
+        val = ws * steps * wbytes * len(Ms) / (ms / 1e3) / 1e9
+    else:
+        val = ws * steps * sum(metrics.call_flops(M, N, K) for M in Ms) / (ms / 1e3) / 1e12
+    res = {"value": val, "unit": w["unit"], "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": steps, "weights": "device-resident (uploaded once, untimed, as model weights)"}
+    # every step also uploads its weights from pinned host memory
+    pk_h = torch.from_numpy(weights[0]).pin_memory()
+    sc_h = torch.from_numpy(weights[1].view(np.int16) if fmt == "int4" else weights[1]).pin_memory()
+    zr_h = None if weights[2] is None else torch.from_numpy(weights[2]).pin_memory()
+    steps_w = max(1, min(args.steps, 100))
+    ms_w = timed(steps_w, (pk_h, sc_h, zr_h))
+    if w["unit"] == "GB/s":
+        val_w = ws * steps_w * wbytes * len(Ms) / (ms_w / 1e3) / 1e9
+    else:
+        val_w = ws * steps_w * sum(metrics.call_flops(M, N, K) for M in Ms) / (ms_w / 1e3) / 1e12
+    res["with_weight_upload"] = {"value": val_w, "unit": w["unit"],
+                                 "h2d_bytes_per_step": h2d + wbytes * len(Ms), "d2h_bytes_per_step": d2h,
+                                 "steps": steps_w}
+    return res
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle, as it stands, on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    w = BENCH_WORKLOADS[args.workload]
+    A_by_M, weights = host_inputs(w)
+    total = args.steps + args.warmup
+    cols = oracle_rate(w, A_by_M, weights, budget_s=max(0.01, 90.0 / max(total, 1)))
+    for i in range(args.warmup):
+        oracle_step_sample(w, cols, A_by_M, weights, seed=100 + i)
+    t = 0.0
+    covered = 0
+    for i in range(args.steps):
+        dt, cv = oracle_step_sample(w, cols, A_by_M, weights, seed=i)
+        t += dt
+        covered += cv
+    from weight_only_bit_w4a16_gb300 import metrics
+    if w["unit"] == "GB/s":
+        value = covered / t / 1e9
+    else:
+        value = args.steps * sum(metrics.call_flops(M, cols, w["K"]) for M in w["Ms"]) / t / 1e12
+    sample = (f"{cols} of {w['N']} output columns of each call of each step "
+              f"(M={list(w['Ms'])}, K={w['K']})")
+    res = {"impl": "reference", "metric": w["metric"], "value": value, "unit": w["unit"],
+           "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3 / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic",
+           "config": {"workload": args.workload, "format": w["fmt"], "group": w["group"], "M": list(w["Ms"]),
+                      "N": w["N"], "K": w["K"], "out": w["out"]},
+           "cpu_baseline": {"value": value, "unit": w["unit"], "cores": oracle.max_threads(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": w["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+           "gpu_launches": 0}
+    print(json.dumps(res), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS), default="decode_int4")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    args = ap.parse_args(argv)
+    if args.steps < 1 or args.warmup < 0:
+        ap.error("--steps >= 1 and --warmup >= 0")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,123 @@
+/*
+ * wq.h -- C ABI of the GB300 W4A16 dequantise-GEMM library (libwq.so).
+ *
+ * The library computes  C = A . deq(B)^T  on one NVIDIA GB300 (sm_103a):
+ *
+ *   A        (M, K)   bf16 activations, row-major.
+ *   packed   (N, K/2) uint8, two 4-bit codes per byte; byte j of row n holds
+ *            element k = 2j in its LOW nibble and k = 2j+1 in its HIGH
+ *            nibble (KBench megakernel_int4_weight_decode.py spec, "The
+ *            weight format"; TileLang example_dequant_gemm_bf16_fp4_hopper.py,
+ *            simple_dequant_bf16_fp4 indexing).
+ *   scales   (N, K/group), one per group of `group` consecutive k of a row:
+ *              WQ_NVFP4  float8_e4m3fn bytes, group 16; weight = e2m1(code) *
+ *                        |e4m3(scale)| (Matmul2dFp4 Mojo API docs, run /
+ *                        run_smem_decode: scales (N, K/16) float8_e4m3fn,
+ *                        decode_e2m1 * |scale|);
+ *              WQ_MXFP4  e8m0 bytes (2^(E-127), 0xFF = NaN), group 32;
+ *                        weight = e2m1(code) * 2^(E-127) (OCP MX; the
+ *                        TileLang example applies the same power-of-two
+ *                        scale as an exponent offset, _tir_u8_to_f4_to_bf16);
+ *              WQ_INT4   bf16 values, any group that is a multiple of 32
+ *                        (128 in the KBench spec); weight = (code - zero) *
+ *                        scale, the zero point subtracted before the multiply
+ *                        (KBench spec, "The weight format" and Precision).
+ *            e2m1 codes: 1 sign, 2 exponent (bias 1), 1 mantissa, exponent 0
+ *            subnormal: +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}.
+ *   zeros    (N, K/group) uint8 zero points for WQ_INT4 (read as full uint8),
+ *            NULL for the fp4 formats.
+ *   C        (M, N) row-major, bf16 (default) or fp32 (format | WQ_OUT_F32).
+ *
+ * Accumulation is fp32; bf16 output is rounded to nearest even.
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates no device memory per call; it keeps only file-scope device
+ *     state (a status word) and small per-process host caches.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*, NULL = the legacy default stream); the call returns once it is
+ *     enqueued.  Launch failures return WQ_ERR_CUDA; faults during execution
+ *     surface at the caller's next synchronisation; a bounded device-side
+ *     wait that ran out is reported by wq_get_device_error().
+ *   - Shapes: M, N >= 0 (M == 0 or N == 0 is a no-op returning WQ_OK);
+ *     K >= 0, a multiple of 32 and of `group`; group as listed above.
+ *     Otherwise WQ_ERR_UNSUPPORTED (shape) or WQ_ERR_INVALID_ARG.
+ *   - A, packed and C must be 16-byte aligned (WQ_ERR_ALIGN otherwise);
+ *     scales 2-byte aligned for WQ_INT4.
+ *   - Arguments are validated before anything is launched; no C++ exception
+ *     crosses this boundary, and there is no CPU path.
+ *   - Calls are thread-safe for distinct streams; calls on one stream run in
+ *     order.
+ */
+#ifndef WQ_H
+#define WQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* weight formats: the low byte of `format` */
+#define WQ_NVFP4 0
+#define WQ_MXFP4 1
+#define WQ_INT4 2
+/* OR into `format`: write C as fp32 instead of bf16 */
+#define WQ_OUT_F32 0x100
+
+/* kernel selection for wq_gemm_ex */
+#define WQ_PATH_AUTO 0 /* M <= 16: split-K GEMV; larger M: tensor-core path */
+#define WQ_PATH_GEMV 1 /* register-decode GEMV kernel, any M (16 rows per pass) */
+#define WQ_PATH_TC 2   /* tcgen05 / TMEM tensor-core kernel */
+
+/* status codes */
+#define WQ_OK 0
+#define WQ_ERR_INVALID_ARG (-1)  /* NULL pointer, negative size, bad format/path */
+#define WQ_ERR_UNSUPPORTED (-2)  /* shape / group the kernels do not handle */
+#define WQ_ERR_ALIGN (-3)        /* pointer alignment */
+#define WQ_ERR_CUDA (-4)         /* a CUDA runtime call or launch failed */
+#define WQ_ERR_DEVICE_TIMEOUT (-5) /* a bounded device-side wait ran out */
+
+/*
+ * wq_gemm -- C = A . deq(packed, scales, zeros)^T on the legacy default
+ * stream with automatic kernel selection.  Arguments as in the header
+ * comment.  Returns a status code.
+ */
+int wq_gemm(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
+            void* C, int M, int N, int K, int format, int group);
+
+/*
+ * wq_gemm_ex -- wq_gemm on an explicit stream (cudaStream_t as void*) with
+ * an explicit kernel choice (WQ_PATH_*).  WQ_PATH_TC returns
+ * WQ_ERR_UNSUPPORTED for shapes that kernel does not take (K not a
+ * multiple of 64, or row strides not 16-byte aligned for TMA).
+ */
+int wq_gemm_ex(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
+               void* C, int M, int N, int K, int format, int group, void* stream, int path);
+
+/*
+ * wq_dequant -- W = deq(packed, scales, zeros) as an (N, K) row-major bf16
+ * matrix, each weight rounded to nearest even from its exact value (so the
+ * result equals the oracle's bf16 image bit for bit; NaN stays NaN, overflow
+ * goes to +-inf, the sign of zero follows the IEEE product).  W must be
+ * 16-byte aligned.  `format` takes no WQ_OUT_F32 flag.
+ */
+int wq_dequant(const uint8_t* packed, const void* scales, const uint8_t* zeros, void* W,
+               int N, int K, int format, int group, void* stream);
+
+/* Returns the device status word (WQ_OK or WQ_ERR_DEVICE_TIMEOUT) of the
+ * current device and clears it.  Synchronises the device. */
+int wq_get_device_error(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* wq_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int wq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WQ_H */

@@ -1,0 +1,103 @@
+"""The C ABI on a machine without a GPU: the library loads, exports every
+entry point include/wq.h declares, and rejects bad arguments before touching
+CUDA (no compute calls are made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import weight_only_bit_w4a16_gb300 as wq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wq.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(wq_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted(wq.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol():
+    L = wq.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_header_constants_match_binding():
+    text = open(HEADER).read()
+    consts = dict(re.findall(r"#define\s+(WQ_[A-Z0-9_]+)\s+\(?(-?(?:0x)?[0-9A-Fa-f]+)\)?", text))
+    for k, v in consts.items():
+        assert getattr(wq, k) == int(v, 0), k
+
+
+def test_status_strings_and_version():
+    for st in (wq.WQ_OK, wq.WQ_ERR_INVALID_ARG, wq.WQ_ERR_UNSUPPORTED, wq.WQ_ERR_ALIGN,
+               wq.WQ_ERR_CUDA, wq.WQ_ERR_DEVICE_TIMEOUT):
+        assert wq.wq_status_string(st).startswith("WQ_")
+    assert wq.wq_status_string(12345) == "unknown wq status"
+    assert wq.wq_version() >= 100
+
+
+# Arguments rejected during validation: nothing reaches CUDA.
+FAKE = ctypes.c_void_p(0x10000)   # 16-byte aligned, never dereferenced
+ODD = ctypes.c_void_p(0x10008)
+
+
+@pytest.mark.parametrize("args,expect", [
+    # (A, packed, scales, zeros, C, M, N, K, format, group)
+    ((FAKE, FAKE, FAKE, None, FAKE, 4, 8, 64, 7, 16), wq.WQ_ERR_INVALID_ARG),       # bad format
+    ((FAKE, FAKE, FAKE, None, FAKE, 4, 8, 64, 0x200, 16), wq.WQ_ERR_INVALID_ARG),   # bad flag
+    ((FAKE, FAKE, FAKE, None, FAKE, -1, 8, 64, 0, 16), wq.WQ_ERR_INVALID_ARG),      # M < 0
+    ((FAKE, FAKE, FAKE, None, FAKE, 4, -8, 64, 0, 16), wq.WQ_ERR_INVALID_ARG),      # N < 0
+    ((FAKE, FAKE, FAKE, None, FAKE, 4, 8, 64, 0, 32), wq.WQ_ERR_UNSUPPORTED),       # nvfp4 group
+    ((FAKE, FAKE, FAKE, None, FAKE, 4, 8, 64, 1, 16), wq.WQ_ERR_UNSUPPORTED),       # mxfp4 group
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, 256, 2, 48), wq.WQ_ERR_UNSUPPORTED),      # int4 group
+    ((FAKE, FAKE, FAKE, None, FAKE, 4, 8, 48, 0, 16), wq.WQ_ERR_UNSUPPORTED),       # K % 32
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, 192, 2, 128), wq.WQ_ERR_UNSUPPORTED),     # K % group
+    ((FAKE, FAKE, FAKE, None, FAKE, 4, 8, 64, 2, 32), wq.WQ_ERR_INVALID_ARG),       # int4 w/o zeros
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, 64, 0, 16), wq.WQ_ERR_INVALID_ARG),       # fp4 with zeros
+    ((FAKE, None, FAKE, None, FAKE, 4, 8, 64, 0, 16), wq.WQ_ERR_INVALID_ARG),       # NULL packed
+    ((FAKE, FAKE, None, None, FAKE, 4, 8, 64, 0, 16), wq.WQ_ERR_INVALID_ARG),       # NULL scales
+    ((None, FAKE, FAKE, None, FAKE, 4, 8, 64, 0, 16), wq.WQ_ERR_INVALID_ARG),       # NULL A
+    ((FAKE, FAKE, FAKE, None, None, 4, 8, 64, 0, 16), wq.WQ_ERR_INVALID_ARG),       # NULL C
+    ((ODD, FAKE, FAKE, None, FAKE, 4, 8, 64, 0, 16), wq.WQ_ERR_ALIGN),              # A alignment
+    ((FAKE, ODD, FAKE, None, FAKE, 4, 8, 64, 0, 16), wq.WQ_ERR_ALIGN),              # packed alignment
+    ((FAKE, FAKE, FAKE, None, ODD, 4, 8, 64, 0, 16), wq.WQ_ERR_ALIGN),              # C alignment
+    ((FAKE, FAKE, ctypes.c_void_p(0x10001), FAKE, FAKE, 4, 8, 64, 2, 32), wq.WQ_ERR_ALIGN),  # int4 scales
+    ((FAKE, FAKE, FAKE, None, FAKE, 0, 8, 64, 0, 16), wq.WQ_OK),                    # M == 0: no-op
+    ((FAKE, FAKE, FAKE, None, FAKE, 4, 0, 64, 0, 16), wq.WQ_OK),                    # N == 0: no-op
+])
+def test_gemm_argument_validation(args, expect):
+    assert wq.wq_gemm(*args) == expect
+    assert wq.wq_gemm_ex(*args, None, wq.WQ_PATH_GEMV) == expect
+
+
+def test_gemm_bad_path():
+    assert wq.wq_gemm_ex(FAKE, FAKE, FAKE, None, FAKE, 4, 8, 64, 0, 16, None, 9) == wq.WQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args,expect", [
+    # (packed, scales, zeros, W, N, K, format, group, stream)
+    ((FAKE, FAKE, None, FAKE, 8, 64, 0x100, 16, None), wq.WQ_ERR_INVALID_ARG),   # output flag
+    ((FAKE, FAKE, None, None, 8, 64, 0, 16, None), wq.WQ_ERR_INVALID_ARG),       # NULL W
+    ((FAKE, FAKE, None, ODD, 8, 64, 0, 16, None), wq.WQ_ERR_ALIGN),              # W alignment
+    ((FAKE, FAKE, None, FAKE, 8, 40, 0, 16, None), wq.WQ_ERR_UNSUPPORTED),       # K % 32
+    ((FAKE, FAKE, None, FAKE, 0, 64, 0, 16, None), wq.WQ_OK),                    # N == 0
+])
+def test_dequant_argument_validation(args, expect):
+    assert wq.wq_dequant(*args) == expect
+
+
+def test_tensor_helpers_refuse_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    A = torch.zeros((1, 64), dtype=torch.bfloat16)
+    packed = torch.zeros((8, 32), dtype=torch.uint8)
+    scales = torch.zeros((8, 4), dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        wq.gemm(A, packed, scales, None, "nvfp4")

@@ -1,0 +1,193 @@
+"""GEMM parity on the GPU: wq_gemm / wq_gemm_ex against the oracle.
+
+Every output element is checked against the oracle's exact fp64 result with
+the method's gate.  The workloads are the seeded synthetic inputs of
+weight_only_bit_w4a16_gb300.synth at their full sizes (sampled rows and
+columns where the oracle would take too long for every element), ragged
+shapes around every tile edge, exact invariants (one-hot activations, sign
+flip, power-of-two scale, zero weights) and determinism.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import weight_only_bit_w4a16_gb300 as wq
+from weight_only_bit_w4a16_gb300 import synth
+
+from gpu_util import (assert_parity, check_full, check_sampled, gpu_gemm, oracle_ref, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+# -- the workloads at full size ------------------------------------------------
+def test_tiny_nvfp4_fp32_out():
+    p = synth.workload_problem("tiny_nvfp4")
+    check_full(p, "fp32", what="tiny_nvfp4")
+    check_full(p, "fp32", path="gemv", what="tiny_nvfp4 gemv")
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_decode_int4(M, seed):
+    p = synth.workload_problem("decode_int4", M=M, seed=seed)
+    check_full(p, "bf16", what=f"decode_int4 M={M}")
+
+
+def test_prefill_mxfp4():
+    p = synth.workload_problem("prefill_mxfp4")
+    check_sampled(p, "bf16", what="prefill_mxfp4")
+
+
+def test_large_nvfp4():
+    p = synth.workload_problem("large_nvfp4")
+    check_sampled(p, "bf16", k=16, what="large_nvfp4")
+
+
+@pytest.mark.parametrize("layer", list(synth.LAYER_SHAPES))
+@pytest.mark.parametrize("M", [1, 16, 128, 2048])
+def test_layer_sweep(layer, M):
+    if layer == "lm_head" and M == 2048:
+        pytest.skip("covered at M=128; 2048 x 128256 output is 0.5 GB")
+    p = synth.layer_problem(layer, M)
+    if M <= 16:
+        check_sampled(p, "bf16", k=8, what=f"{layer} M={M}")
+    else:
+        check_sampled(p, "bf16", k=8, what=f"{layer} M={M}")
+
+
+# -- both kernels on the same shapes ------------------------------------------
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "int4"])
+@pytest.mark.parametrize("path", ["gemv", "auto"])
+@pytest.mark.parametrize("M", [1, 5, 8, 9, 16, 17, 40, 128, 300])
+def test_paths_agree_with_oracle(fmt, path, M):
+    p = synth.make_problem(fmt, M, 384, 1024, seed=M)
+    out = "fp32" if M % 2 else "bf16"
+    check_full(p, out, path=path, what=f"{fmt} M={M} {path}")
+
+
+# -- ragged shapes ---------------------------------------------------------------
+@pytest.mark.parametrize("M", list(range(1, 18)) + [127, 129])
+def test_ragged_M(M):
+    p = synth.make_problem("int4", M, 200, 640, seed=100 + M)
+    check_full(p, "fp32", what=f"ragged M={M}")
+
+
+@pytest.mark.parametrize("N", [1, 7, 15, 16, 17, 100, 257, 1000])
+@pytest.mark.parametrize("fmt", ["nvfp4", "int4"])
+def test_ragged_N(N, fmt):
+    for M in (3, 16, 200):
+        p = synth.make_problem(fmt, M, N, 512, seed=N + M)
+        check_full(p, "bf16", what=f"{fmt} N={N} M={M}")
+
+
+@pytest.mark.parametrize("K", [32, 64, 96, 160, 1056, 4160])
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+def test_ragged_K(K, fmt):
+    for M in (2, 130):
+        p = synth.make_problem(fmt, M, 96, K, seed=K + M)
+        check_full(p, "fp32", what=f"{fmt} K={K} M={M}")
+
+
+@pytest.mark.parametrize("group", [32, 64, 96, 128, 256])
+def test_int4_group_sizes(group):
+    K = 768
+    for M in (4, 64):
+        p = synth.make_problem("int4", M, 160, K, group=group, seed=group)
+        check_full(p, "fp32", what=f"int4 g{group} M={M}")
+
+
+def test_zero_K_gives_zeros():
+    dev = torch.device("cuda:0")
+    A = torch.zeros((4, 0), dtype=torch.bfloat16, device=dev)
+    packed = torch.zeros((8, 0), dtype=torch.uint8, device=dev)
+    scales = torch.zeros((8, 0), dtype=torch.uint8, device=dev)
+    C = torch.full((4, 8), 5.0, device=dev)
+    st = wq.wq_gemm_ex(A.data_ptr() or 0x10000, packed.data_ptr() or 0x10000, scales.data_ptr() or 0x10000,
+                       None, C.data_ptr(), 4, 8, 0, wq.WQ_NVFP4 | wq.WQ_OUT_F32, 16,
+                       torch.cuda.current_stream().cuda_stream, wq.WQ_PATH_AUTO)
+    torch.cuda.synchronize()
+    assert st == wq.WQ_OK
+    assert torch.all(C == 0)
+
+
+# -- exact invariants (fp32 output) ---------------------------------------------
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "int4"])
+@pytest.mark.parametrize("path", ["gemv", "auto"])
+def test_one_hot_activation_selects_weight(fmt, path):
+    K = 512
+    p = synth.make_problem(fmt, 1, 64, K, seed=3)
+    ks = np.array([0, 1, 2, 31, 32, 127, 128, 300, 511] + list(range(40, 80)))
+    A = np.zeros((len(ks), K), dtype=np.uint16)
+    A[np.arange(len(ks)), ks] = 0x3F80
+    p["A"], p["M"] = A, len(ks)
+    C = gpu_gemm(p, "fp32", path)
+    W64, Wb = oracle.dequant(p["packed"], p["scales"], p["zeros"], fmt, p["group"])
+    w64 = W64[:, ks].T
+    wbf = np.asarray(
+        torch.from_numpy(Wb[:, ks].T.astype(np.int16).copy()).view(torch.bfloat16).float().numpy(),
+        dtype=np.float64)
+    # fp4 weights are exact in bf16; int4 weights are either exact (scale
+    # applied in fp32 after the MMA) or their bf16 image
+    assert np.all((C == w64) | (C == wbf))
+    if fmt != "int4":
+        assert np.array_equal(C, w64)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("M", [3, 200])
+def test_sign_flip_negates_exactly(fmt, M):
+    p = synth.make_problem(fmt, M, 128, 512, seed=7)
+    C = gpu_gemm(p, "fp32")
+    q = dict(p, packed=p["packed"] ^ 0x88)
+    C2 = gpu_gemm(q, "fp32")
+    assert np.array_equal(C2, -C)
+
+
+@pytest.mark.parametrize("M", [3, 200])
+def test_mxfp4_exponent_plus_one_doubles_exactly(M):
+    p = synth.make_problem("mxfp4", M, 128, 512, seed=8)
+    C = gpu_gemm(p, "fp32")
+    C2 = gpu_gemm(dict(p, scales=p["scales"] + 1), "fp32")
+    assert np.array_equal(C2, 2 * C)
+
+
+@pytest.mark.parametrize("M", [4, 64])
+def test_int4_codes_equal_zero_give_zero(M):
+    N, K, g = 96, 512, 128
+    rng = np.random.default_rng(5)
+    z = rng.integers(0, 16, size=(N, K // g), dtype=np.uint8)
+    codes = np.repeat(z, g, axis=1)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    p = synth.make_problem("int4", M, N, K, seed=5)
+    p.update(packed=packed, zeros=z)
+    assert np.all(gpu_gemm(p, "fp32") == 0)
+
+
+def test_nvfp4_zero_scale_gives_zero():
+    p = synth.make_problem("nvfp4", 40, 64, 256, seed=6)
+    p["scales"] = np.zeros_like(p["scales"])
+    assert np.all(gpu_gemm(p, "fp32") == 0)
+
+
+# -- determinism, streams, output bounds ---------------------------------------
+@pytest.mark.parametrize("M", [16, 256])
+def test_deterministic(M):
+    p = synth.make_problem("int4", M, 1024, 3072, seed=9)
+    C1 = gpu_gemm(p, "fp32")
+    C2 = gpu_gemm(p, "fp32")
+    assert np.array_equal(C1, C2)
+
+
+def test_side_stream_and_guard_region():
+    p = synth.make_problem("nvfp4", 12, 72, 256, seed=10)
+    A, packed, scales, zeros = to_dev(p)
+    buf = torch.full((12 * 72 + 256,), 3.0, device="cuda")
+    C = buf[: 12 * 72].view(12, 72)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        wq.gemm(A, packed, scales, zeros, "nvfp4", out_dtype="fp32", out=C)
+    s.synchronize()
+    assert torch.all(buf[12 * 72:] == 3.0)
+    Ce, S = oracle_ref(p)
+    assert_parity(C.cpu().numpy().astype(np.float64), Ce, S, "fp32", "side stream")

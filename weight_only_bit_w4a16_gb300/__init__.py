@@ -1,0 +1,179 @@
+"""Python binding of libwq.so, the GB300 W4A16 dequantise-GEMM library.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in include/wq.h.  There is no CPU path --
+if the compiled library is missing, every call raises.
+
+Low level (same names as the C ABI, integer pointers):
+    wq_gemm, wq_gemm_ex, wq_dequant, wq_get_device_error, wq_status_string,
+    wq_version
+Tensor level (torch CUDA tensors, raises WQError on a non-OK status):
+    gemm(A, packed, scales, zeros, fmt, group=None, out_dtype="bf16", ...)
+    dequant(packed, scales, zeros, fmt, group=None, out=None, ...)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libwq.so")
+
+# constants of include/wq.h
+WQ_NVFP4, WQ_MXFP4, WQ_INT4 = 0, 1, 2
+WQ_OUT_F32 = 0x100
+WQ_PATH_AUTO, WQ_PATH_GEMV, WQ_PATH_TC = 0, 1, 2
+WQ_OK = 0
+WQ_ERR_INVALID_ARG = -1
+WQ_ERR_UNSUPPORTED = -2
+WQ_ERR_ALIGN = -3
+WQ_ERR_CUDA = -4
+WQ_ERR_DEVICE_TIMEOUT = -5
+
+FORMATS = {"nvfp4": WQ_NVFP4, "mxfp4": WQ_MXFP4, "int4": WQ_INT4}
+DEFAULT_GROUP = {"nvfp4": 16, "mxfp4": 32, "int4": 128}
+PATHS = {"auto": WQ_PATH_AUTO, "gemv": WQ_PATH_GEMV, "tc": WQ_PATH_TC}
+
+#: the C entry points include/wq.h declares: name -> (restype, argtypes)
+_vp, _i = ctypes.c_void_p, ctypes.c_int
+SIGNATURES = {
+    "wq_gemm": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i]),
+    "wq_gemm_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i]),
+    "wq_dequant": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "wq_get_device_error": (_i, []),
+    "wq_status_string": (ctypes.c_char_p, [_i]),
+    "wq_version": (_i, []),
+}
+
+
+class WQError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})" if what else status_string(status))
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libwq.so (built by __graft_entry__.build() / build.py); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`"
+                    " (there is no CPU fallback)")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+    return _lib
+
+
+# -- the C ABI, same names ----------------------------------------------------
+def wq_gemm(A, packed, scales, zeros, C, M, N, K, format, group) -> int:
+    return lib().wq_gemm(A, packed, scales, zeros, C, M, N, K, format, group)
+
+
+def wq_gemm_ex(A, packed, scales, zeros, C, M, N, K, format, group, stream, path) -> int:
+    return lib().wq_gemm_ex(A, packed, scales, zeros, C, M, N, K, format, group, stream, path)
+
+
+def wq_dequant(packed, scales, zeros, W, N, K, format, group, stream) -> int:
+    return lib().wq_dequant(packed, scales, zeros, W, N, K, format, group, stream)
+
+
+def wq_get_device_error() -> int:
+    return lib().wq_get_device_error()
+
+
+def wq_status_string(status: int) -> str:
+    return lib().wq_status_string(int(status)).decode()
+
+
+def wq_version() -> int:
+    return lib().wq_version()
+
+
+def status_string(status: int) -> str:
+    try:
+        return wq_status_string(status)
+    except Exception:   # library not loadable: still give a message
+        return f"wq status {status}"
+
+
+# -- tensor-level helpers -------------------------------------------------------
+def _fmt(fmt) -> int:
+    return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def _fmt_name(fmt) -> str:
+    if isinstance(fmt, str):
+        return fmt
+    return {v: k for k, v in FORMATS.items()}[int(fmt)]
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device):
+    import torch
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def gemm(A, packed, scales, zeros, fmt, group=None, out_dtype="bf16", out=None, path="auto", stream=None):
+    """C = A . deq(packed, scales, zeros)^T on A's device and current stream.
+
+    A: (M, K) bf16; packed: (N, K/2) uint8; scales: (N, K/group) uint8
+    (nvfp4 e4m3 / mxfp4 e8m0 bytes) or bf16 (int4); zeros: (N, K/group)
+    uint8 for int4, None otherwise.  Returns C (M, N) bf16 or fp32.
+    """
+    import torch
+    f = _fmt(fmt)
+    group = group or DEFAULT_GROUP[_fmt_name(fmt)]
+    M, K = A.shape
+    N = packed.shape[0]
+    if packed.shape[1] * 2 != K:
+        raise ValueError(f"packed {tuple(packed.shape)} does not match K={K}")
+    for t in (A, packed, scales, zeros, out):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    if A.dtype != torch.bfloat16 or packed.dtype != torch.uint8:
+        raise ValueError("A must be bf16 and packed uint8")
+    odt = torch.float32 if out_dtype in ("fp32", torch.float32) else torch.bfloat16
+    if out is None:
+        out = torch.empty((M, N), dtype=odt, device=A.device)
+    elif out.shape != (M, N) or out.dtype != odt:
+        raise ValueError("out has the wrong shape or dtype")
+    fmt_word = f | (WQ_OUT_F32 if odt == torch.float32 else 0)
+    st = wq_gemm_ex(_ptr(A), _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(out), M, N, K, fmt_word,
+                    int(group), _stream_handle(stream, A.device), PATHS[path] if isinstance(path, str) else path)
+    if st != WQ_OK:
+        raise WQError(st, "wq_gemm_ex")
+    return out
+
+
+def dequant(packed, scales, zeros, fmt, group=None, out=None, stream=None):
+    """W = deq(packed, scales, zeros) as an (N, K) bf16 tensor (bit-exact RNE)."""
+    import torch
+    f = _fmt(fmt)
+    group = group or DEFAULT_GROUP[_fmt_name(fmt)]
+    N, Kh = packed.shape
+    K = 2 * Kh
+    for t in (packed, scales, zeros, out):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.bfloat16, device=packed.device)
+    st = wq_dequant(_ptr(packed), _ptr(scales), _ptr(zeros), _ptr(out), N, K, f, int(group),
+                    _stream_handle(stream, packed.device))
+    if st != WQ_OK:
+        raise WQError(st, "wq_dequant")
+    return out

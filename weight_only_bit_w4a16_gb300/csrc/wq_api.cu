@@ -1,0 +1,94 @@
+// wq_api.cu -- the C ABI (include/wq.h): argument validation and kernel
+// selection.  Nothing here computes; every step of the product runs in the
+// kernels of wq_dequant.cu, wq_gemv.cu and wq_tc.cu.
+#include <cstdint>
+
+#include "wq_internal.h"
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Shared checks of the weight description.  Returns WQ_OK or an error code.
+int check_weights(const uint8_t* packed, const void* scales, const uint8_t* zeros, int N, int K,
+                  int fmt, int group) {
+    if (N < 0 || K < 0) return WQ_ERR_INVALID_ARG;
+    if (fmt != WQ_NVFP4 && fmt != WQ_MXFP4 && fmt != WQ_INT4) return WQ_ERR_INVALID_ARG;
+    if (group <= 0) return WQ_ERR_INVALID_ARG;
+    if (fmt == WQ_NVFP4 && group != 16) return WQ_ERR_UNSUPPORTED;
+    if (fmt == WQ_MXFP4 && group != 32) return WQ_ERR_UNSUPPORTED;
+    if (fmt == WQ_INT4 && group % 32 != 0) return WQ_ERR_UNSUPPORTED;
+    if (K % 32 != 0 || K % group != 0) return WQ_ERR_UNSUPPORTED;
+    if (N > 0 && K > 0) {
+        if (!packed || !scales) return WQ_ERR_INVALID_ARG;
+        if (fmt == WQ_INT4 && !zeros) return WQ_ERR_INVALID_ARG;
+        if (fmt != WQ_INT4 && zeros) return WQ_ERR_INVALID_ARG;
+        if (!aligned(packed, 16)) return WQ_ERR_ALIGN;
+        if (fmt == WQ_INT4 && !aligned(scales, 2)) return WQ_ERR_ALIGN;
+    }
+    return WQ_OK;
+}
+
+}  // namespace
+
+#define WQ_EXPORT __attribute__((visibility("default")))
+
+extern "C" {
+
+WQ_EXPORT int wq_gemm_ex(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C,
+               int M, int N, int K, int format, int group, void* stream, int path) {
+    if (format & ~(0xFF | WQ_OUT_F32)) return WQ_ERR_INVALID_ARG;
+    const int fmt = format & 0xFF;
+    const bool out_f32 = (format & WQ_OUT_F32) != 0;
+    if (M < 0) return WQ_ERR_INVALID_ARG;
+    if (path != WQ_PATH_AUTO && path != WQ_PATH_GEMV && path != WQ_PATH_TC) return WQ_ERR_INVALID_ARG;
+    int st = check_weights(packed, scales, zeros, N, K, fmt, group);
+    if (st != WQ_OK) return st;
+    if (M == 0 || N == 0) return WQ_OK;
+    if (!C || (K > 0 && !A)) return WQ_ERR_INVALID_ARG;
+    if (!aligned(C, 16) || (K > 0 && !aligned(A, 16))) return WQ_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (path == WQ_PATH_TC)
+        return wq::launch_tc(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, s);
+    if (path == WQ_PATH_AUTO && M > 16 && K > 0) {
+        st = wq::launch_tc(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, s);
+        if (st != WQ_ERR_UNSUPPORTED) return st;
+        // shapes the tensor-core kernel does not take run on the GEMV kernel
+    }
+    return wq::launch_gemv(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, s);
+}
+
+WQ_EXPORT int wq_gemm(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C, int M,
+            int N, int K, int format, int group) {
+    return wq_gemm_ex(A, packed, scales, zeros, C, M, N, K, format, group, nullptr, WQ_PATH_AUTO);
+}
+
+WQ_EXPORT int wq_dequant(const uint8_t* packed, const void* scales, const uint8_t* zeros, void* W, int N, int K,
+               int format, int group, void* stream) {
+    if (format & ~0xFF) return WQ_ERR_INVALID_ARG;
+    const int st = check_weights(packed, scales, zeros, N, K, format, group);
+    if (st != WQ_OK) return st;
+    if (N == 0 || K == 0) return WQ_OK;
+    if (!W) return WQ_ERR_INVALID_ARG;
+    if (!aligned(W, 16)) return WQ_ERR_ALIGN;
+    return wq::launch_dequant(packed, scales, zeros, W, N, K, format, group, static_cast<cudaStream_t>(stream));
+}
+
+WQ_EXPORT int wq_get_device_error(void) { return wq::read_and_clear_device_status(); }
+
+WQ_EXPORT const char* wq_status_string(int status) {
+    switch (status) {
+        case WQ_OK: return "WQ_OK";
+        case WQ_ERR_INVALID_ARG: return "WQ_ERR_INVALID_ARG: null pointer, negative size or bad format/path";
+        case WQ_ERR_UNSUPPORTED: return "WQ_ERR_UNSUPPORTED: shape or group not handled by the kernels";
+        case WQ_ERR_ALIGN: return "WQ_ERR_ALIGN: pointer not aligned as required";
+        case WQ_ERR_CUDA: return "WQ_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+        case WQ_ERR_DEVICE_TIMEOUT: return "WQ_ERR_DEVICE_TIMEOUT: a bounded device-side wait ran out";
+        default: return "unknown wq status";
+    }
+}
+
+WQ_EXPORT int wq_version(void) { return 100; }
+
+}  // extern "C"

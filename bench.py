@@ -276,22 +276,27 @@ def run_ours(args):
     C_d = {M: torch.empty((M, N), dtype=odt, device=dev) for M in Ms}
     s = torch.cuda.Stream(dev)
 
-    def call(M, slot, stream_handle):
+    # the weights are never written by the kernels of the step, so every call
+    # may overlap the previous one (WQ_LAUNCH_OVERLAP, programmatic dependent
+    # launch); the plain launch is timed as well and reported beside it
+    overlap = wq.WQ_LAUNCH_OVERLAP if not args.no_overlap else 0
+
+    def call(M, slot, stream_handle, flags=None):
         pk, sc, zr = pool[slot]
         st = wq.wq_gemm_ex(A_d[M].data_ptr(), pk.data_ptr(), sc.data_ptr(),
                            None if zr is None else zr.data_ptr(), C_d[M].data_ptr(), M, N, K, fcode, group,
-                           stream_handle, wq.WQ_PATH_AUTO)
+                           stream_handle, wq.WQ_PATH_AUTO | (overlap if flags is None else flags))
         if st != wq.WQ_OK:
             raise wq.WQError(st, "wq_gemm_ex")
 
-    def capture(nsteps, Ms_used):
+    def capture(nsteps, Ms_used, flags=None):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(s):
             with torch.cuda.graph(g, stream=s):
                 h = torch.cuda.current_stream().cuda_stream
                 for i in range(nsteps):
                     for j, M in enumerate(Ms_used):
-                        call(M, (i * len(Ms_used) + j) % R, h)
+                        call(M, (i * len(Ms_used) + j) % R, h, flags)
         return g
 
     # graphs of G steps; G * len(Ms) is a multiple of R so replays rotate seamlessly
@@ -355,6 +360,19 @@ def run_ours(args):
                 "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
                 "algorithmic_flops_per_launch": algo, "peak_source": peaks["source"] + " bf16_tflops (burst)"}
 
+    # the same steps with plain launches (no overlap), not part of the value
+    g_plain = capture(G, Ms, flags=0)
+    g_plain.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(max(1, args.steps // G)):
+            g_plain.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    plain_ms_per_step = e0.elapsed_time(e1) / (max(1, args.steps // G) * G)
+
     # per-M launch time (separate graphs of one M; not part of the timed steps)
     per_m = {}
     if w["bound"] == "hbm" and len(Ms) > 1:
@@ -387,8 +405,13 @@ def run_ours(args):
                    "l2": f"inputs larger than L2: {R} weight sets of {wb / 1e6:.2f} MB rotated "
                          f"({R * wb / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
                    "timing": "CUDA graphs of the timed steps, CUDA events on the launching stream",
+                   "launch": "WQ_LAUNCH_OVERLAP (programmatic dependent launch)" if overlap else "plain",
                    "parallelism": f"replicas x{ws}"},
         "roofline": roof, "clocks": clocks, "gpu_launches": launches, "e2e": e2e,
+        "plain_launch": {"ms_per_step": plain_ms_per_step,
+                         "value": ws * (per_step_w if w["bound"] == "hbm" else
+                                        sum(metrics.call_flops(M, N, K) for M in Ms)) /
+                                  (plain_ms_per_step / 1e3) / (1e9 if w["bound"] == "hbm" else 1e12)},
     }
     if per_m:
         result["per_m"] = per_m
@@ -517,6 +540,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS), default="decode_int4")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="time plain launches instead of WQ_LAUNCH_OVERLAP")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     args = ap.parse_args(argv)

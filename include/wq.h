@@ -66,10 +66,16 @@ extern "C" {
 /* OR into `format`: write C as fp32 instead of bf16 */
 #define WQ_OUT_F32 0x100
 
-/* kernel selection for wq_gemm_ex */
+/* kernel selection for wq_gemm_ex: the low byte of `path` */
 #define WQ_PATH_AUTO 0 /* M <= 16: split-K GEMV; larger M: tensor-core path */
 #define WQ_PATH_GEMV 1 /* register-decode GEMV kernel, any M (16 rows per pass) */
 #define WQ_PATH_TC 2   /* tcgen05 / TMEM tensor-core kernel */
+/* OR into `path`: launch with programmatic dependent launch, so that the
+ * GEMV kernel starts streaming its weights while the preceding kernel on the
+ * stream is still running (A is read and C written only after that kernel
+ * has completed).  The caller guarantees that the preceding kernel does not
+ * write packed, scales or zeros -- true whenever they are model weights. */
+#define WQ_LAUNCH_OVERLAP 0x100
 
 /* status codes */
 #define WQ_OK 0
@@ -89,9 +95,9 @@ int wq_gemm(const void* A, const uint8_t* packed, const void* scales, const uint
 
 /*
  * wq_gemm_ex -- wq_gemm on an explicit stream (cudaStream_t as void*) with
- * an explicit kernel choice (WQ_PATH_*).  WQ_PATH_TC returns
- * WQ_ERR_UNSUPPORTED for shapes that kernel does not take (K not a
- * multiple of 64, or row strides not 16-byte aligned for TMA).
+ * an explicit kernel choice (WQ_PATH_*, optionally | WQ_LAUNCH_OVERLAP).
+ * WQ_PATH_TC returns WQ_ERR_UNSUPPORTED for shapes that kernel does not take
+ * (K not a multiple of 64, or row strides not 16-byte aligned for TMA).
  */
 int wq_gemm_ex(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
                void* C, int M, int N, int K, int format, int group, void* stream, int path);

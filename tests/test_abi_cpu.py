@@ -80,6 +80,10 @@ def test_gemm_argument_validation(args, expect):
 
 def test_gemm_bad_path():
     assert wq.wq_gemm_ex(FAKE, FAKE, FAKE, None, FAKE, 4, 8, 64, 0, 16, None, 9) == wq.WQ_ERR_INVALID_ARG
+    assert wq.wq_gemm_ex(FAKE, FAKE, FAKE, None, FAKE, 4, 8, 64, 0, 16, None, 0x200) == wq.WQ_ERR_INVALID_ARG
+    # the overlap flag is a valid path bit (M == 0: validated, nothing launched)
+    assert wq.wq_gemm_ex(FAKE, FAKE, FAKE, None, FAKE, 0, 8, 64, 0, 16, None,
+                         wq.WQ_PATH_GEMV | wq.WQ_LAUNCH_OVERLAP) == wq.WQ_OK
 
 
 @pytest.mark.parametrize("args,expect", [

@@ -191,3 +191,46 @@ def test_side_stream_and_guard_region():
     assert torch.all(buf[12 * 72:] == 3.0)
     Ce, S = oracle_ref(p)
     assert_parity(C.cpu().numpy().astype(np.float64), Ce, S, "fp32", "side stream")
+
+
+# -- launch options -------------------------------------------------------------
+def test_overlapped_launches_chain_correctly():
+    """WQ_LAUNCH_OVERLAP: calls on one stream, each reading the previous
+    call's output as its activations, must still see that output complete."""
+    K = N = 1024
+    ps = [synth.make_problem("int4", 4, N, K, seed=40 + i) for i in range(3)]
+    dev = torch.device("cuda:0")
+    x = torch.from_numpy(ps[0]["A"].view(np.int16)).view(torch.bfloat16).to(dev)
+    outs = []
+    for p in ps:
+        _, packed, scales, zeros = to_dev(p)
+        x = wq.gemm(x, packed, scales, zeros, "int4", overlap=True)
+        outs.append(x)
+    torch.cuda.synchronize()
+    # replay on the host, step by step, through the oracle
+    a_bits = ps[0]["A"]
+    for p, o in zip(ps, outs):
+        q = dict(p, A=a_bits)
+        Ce, S = oracle_ref(q)
+        got = o.float().cpu().numpy().astype(np.float64)
+        assert_parity(got, Ce, S, "bf16", "overlap chain")
+        a_bits = o.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_cluster_kernel_variant(M, monkeypatch):
+    """The cluster-split GEMV (used for large M x K) on the decode shape."""
+    monkeypatch.setenv("WQ_GEMV_FORCE_CLUSTER", "1")
+    p = synth.workload_problem("decode_int4", M=M, seed=3)
+    check_full(p, "bf16", path="gemv", what=f"cluster M={M}")
+    q = synth.make_problem("nvfp4", M, 512, 1024, seed=M)
+    check_full(q, "fp32", path="gemv", what=f"cluster nvfp4 M={M}")
+
+
+@pytest.mark.parametrize("wk", ["0", "1", "2", "3", "4"])
+def test_split_kernel_warp_splits(wk, monkeypatch):
+    """Every K split of the in-CTA split kernel gives the same parity."""
+    monkeypatch.setenv("WQ_GEMV_WK_LOG2", wk)
+    for fmt, M in (("int4", 1), ("int4", 12), ("mxfp4", 3)):
+        p = synth.make_problem(fmt, M, 300, 3072, seed=int(wk) + M)
+        check_full(p, "fp32", path="gemv", what=f"{fmt} wk={wk} M={M}")

@@ -24,6 +24,7 @@ LIB_PATH = os.path.join(_HERE, "libwq.so")
 WQ_NVFP4, WQ_MXFP4, WQ_INT4 = 0, 1, 2
 WQ_OUT_F32 = 0x100
 WQ_PATH_AUTO, WQ_PATH_GEMV, WQ_PATH_TC = 0, 1, 2
+WQ_LAUNCH_OVERLAP = 0x100
 WQ_OK = 0
 WQ_ERR_INVALID_ARG = -1
 WQ_ERR_UNSUPPORTED = -2
@@ -128,8 +129,13 @@ def _stream_handle(stream, device):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def gemm(A, packed, scales, zeros, fmt, group=None, out_dtype="bf16", out=None, path="auto", stream=None):
+def gemm(A, packed, scales, zeros, fmt, group=None, out_dtype="bf16", out=None, path="auto", stream=None,
+         overlap=False):
     """C = A . deq(packed, scales, zeros)^T on A's device and current stream.
+
+    overlap=True sets WQ_LAUNCH_OVERLAP (programmatic dependent launch): the
+    caller guarantees the preceding kernel on the stream does not write the
+    weights.
 
     A: (M, K) bf16; packed: (N, K/2) uint8; scales: (N, K/group) uint8
     (nvfp4 e4m3 / mxfp4 e8m0 bytes) or bf16 (int4); zeros: (N, K/group)
@@ -153,8 +159,9 @@ def gemm(A, packed, scales, zeros, fmt, group=None, out_dtype="bf16", out=None, 
     elif out.shape != (M, N) or out.dtype != odt:
         raise ValueError("out has the wrong shape or dtype")
     fmt_word = f | (WQ_OUT_F32 if odt == torch.float32 else 0)
+    pcode = (PATHS[path] if isinstance(path, str) else int(path)) | (WQ_LAUNCH_OVERLAP if overlap else 0)
     st = wq_gemm_ex(_ptr(A), _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(out), M, N, K, fmt_word,
-                    int(group), _stream_handle(stream, A.device), PATHS[path] if isinstance(path, str) else path)
+                    int(group), _stream_handle(stream, A.device), pcode)
     if st != WQ_OK:
         raise WQError(st, "wq_gemm_ex")
     return out

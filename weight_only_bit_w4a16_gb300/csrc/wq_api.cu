@@ -41,6 +41,9 @@ WQ_EXPORT int wq_gemm_ex(const void* A, const uint8_t* packed, const void* scale
     const int fmt = format & 0xFF;
     const bool out_f32 = (format & WQ_OUT_F32) != 0;
     if (M < 0) return WQ_ERR_INVALID_ARG;
+    if (path & ~(0xFF | WQ_LAUNCH_OVERLAP)) return WQ_ERR_INVALID_ARG;
+    const bool overlap = (path & WQ_LAUNCH_OVERLAP) != 0;
+    path &= 0xFF;
     if (path != WQ_PATH_AUTO && path != WQ_PATH_GEMV && path != WQ_PATH_TC) return WQ_ERR_INVALID_ARG;
     int st = check_weights(packed, scales, zeros, N, K, fmt, group);
     if (st != WQ_OK) return st;
@@ -56,7 +59,7 @@ WQ_EXPORT int wq_gemm_ex(const void* A, const uint8_t* packed, const void* scale
         if (st != WQ_ERR_UNSUPPORTED) return st;
         // shapes the tensor-core kernel does not take run on the GEMV kernel
     }
-    return wq::launch_gemv(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, s);
+    return wq::launch_gemv(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, overlap, s);
 }
 
 WQ_EXPORT int wq_gemm(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C, int M,

@@ -77,22 +77,24 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
         : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
 }
 
+// Loads of read-only inputs (weights and scales never change while a kernel
+// runs): plain asm, so the compiler may schedule and predicate them freely.
 __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
 }
 
 __device__ __forceinline__ uint32_t ldg_u8(const uint8_t* p) {
     uint16_t v;
-    asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
+    asm("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
     return v;
 }
 
 __device__ __forceinline__ uint32_t ldg_u16(const void* p) {
     uint16_t v;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    asm("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
     return v;
 }
 

@@ -12,8 +12,10 @@ namespace wq {
 int launch_dequant(const uint8_t* packed, const void* scales, const uint8_t* zeros, void* W, int N,
                    int K, int fmt, int group, cudaStream_t stream);
 
+// pdl: launch with programmatic dependent launch (the kernel streams its
+// weights before the preceding kernel on the stream has finished)
 int launch_gemv(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
-                void* C, int M, int N, int K, int fmt, int group, bool out_f32, cudaStream_t stream);
+                void* C, int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, cudaStream_t stream);
 
 // Returns WQ_ERR_UNSUPPORTED (without launching) for shapes the tensor-core
 // kernel does not take.

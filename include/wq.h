@@ -116,6 +116,13 @@ int wq_dequant(const uint8_t* packed, const void* scales, const uint8_t* zeros, 
  * current device and clears it.  Synchronises the device. */
 int wq_get_device_error(void);
 
+/* Failure-path self test: enqueues a one-thread kernel whose bounded wait on
+ * an mbarrier that nothing completes runs out after ~20 ms; the kernel then
+ * records WQ_ERR_DEVICE_TIMEOUT exactly as a GEMM kernel would.  Nothing
+ * hangs and the context stays usable; wq_get_device_error() afterwards
+ * returns (and clears) WQ_ERR_DEVICE_TIMEOUT.  Returns a launch status. */
+int wq_selftest_timeout(void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* wq_status_string(int status);
 

@@ -5,8 +5,8 @@ kernels behind the C ABI declared in include/wq.h.  There is no CPU path --
 if the compiled library is missing, every call raises.
 
 Low level (same names as the C ABI, integer pointers):
-    wq_gemm, wq_gemm_ex, wq_dequant, wq_get_device_error, wq_status_string,
-    wq_version
+    wq_gemm, wq_gemm_ex, wq_dequant, wq_get_device_error, wq_selftest_timeout,
+    wq_status_string, wq_version
 Tensor level (torch CUDA tensors, raises WQError on a non-OK status):
     gemm(A, packed, scales, zeros, fmt, group=None, out_dtype="bf16", ...)
     dequant(packed, scales, zeros, fmt, group=None, out=None, ...)
@@ -43,6 +43,7 @@ SIGNATURES = {
     "wq_gemm_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i]),
     "wq_dequant": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "wq_get_device_error": (_i, []),
+    "wq_selftest_timeout": (_i, [_vp]),
     "wq_status_string": (ctypes.c_char_p, [_i]),
     "wq_version": (_i, []),
 }
@@ -91,6 +92,10 @@ def wq_dequant(packed, scales, zeros, W, N, K, format, group, stream) -> int:
 
 def wq_get_device_error() -> int:
     return lib().wq_get_device_error()
+
+
+def wq_selftest_timeout(stream=None) -> int:
+    return lib().wq_selftest_timeout(stream)
 
 
 def wq_status_string(status: int) -> str:

@@ -80,6 +80,10 @@ WQ_EXPORT int wq_dequant(const uint8_t* packed, const void* scales, const uint8_
 
 WQ_EXPORT int wq_get_device_error(void) { return wq::read_and_clear_device_status(); }
 
+WQ_EXPORT int wq_selftest_timeout(void* stream) {
+    return wq::launch_timeout_selftest(static_cast<cudaStream_t>(stream));
+}
+
 WQ_EXPORT const char* wq_status_string(int status) {
     switch (status) {
         case WQ_OK: return "WQ_OK";

@@ -220,6 +220,27 @@ __device__ __forceinline__ void word_scaled(uint32_t w, const GroupKey& key, uin
     }
 }
 
+__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// int4 word as an exact two-term bf16 sum: hi = RNE(w), lo = w - hi.  The
+// weight (code - zero) * scale has at most 13 significant bits, so the
+// residual (at most 6 bits) is a bf16 number and fma(x, s, -hi), which rounds
+// the exact x*s - hi once, returns it exactly: hi + lo == w.
+template <bool TWO>
+__device__ __forceinline__ void int4_word_split(uint32_t w, const GroupKey& key, uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+    uint32_t x[4];
+    int4_word_centered<TWO>(w, key, x);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        hi[i] = bf16x2_mul(x[i], key.mul);
+        lo[i] = bf16x2_fma(x[i], key.mul, hi[i] ^ 0x80008000u);
+    }
+}
+
 // key of group gi from the raw scale / zero arrays
 template <int FMT>
 __device__ __forceinline__ GroupKey load_key(const void* scales, const uint8_t* zeros, size_t gi) {

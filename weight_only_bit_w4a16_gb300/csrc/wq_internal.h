@@ -22,6 +22,9 @@ int launch_gemv(const void* A, const uint8_t* packed, const void* scales, const 
 int launch_tc(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
               void* C, int M, int N, int K, int fmt, int group, bool out_f32, cudaStream_t stream);
 
+// A kernel whose bounded wait is bound to run out (tests the failure path).
+int launch_timeout_selftest(cudaStream_t stream);
+
 // Device status word of the current device: read and clear.
 int read_and_clear_device_status();
 

@@ -1,7 +1,38 @@
-// wq_tc.cu -- the large-M tensor-core path (tcgen05 / TMEM) and the device
-// status word that its bounded waits report into.
+// wq_tc.cu -- the large-M path: TMA-fed, warp-specialised tcgen05 kernel with
+// the dequantised weights in tensor memory, and the device status word that
+// its bounded waits report into.
+//
+// Tile: 128 weight rows (n) x 256 activation rows (m) x all of K, in k-steps
+// of 64.  The product is computed transposed, D = W . A^T, so that the
+// dequantised weights are the A operand of tcgen05.mma and can live in TMEM:
+//   * warp 0, one lane: TMA producer.  Per k-step it loads the activation
+//     tile (256 x 64 bf16, 128-byte swizzle, the MMA's B operand in shared
+//     memory) and the packed weight tile (128 rows x 32 bytes, 32-byte
+//     swizzle) into a ring of kStages stages, completing on the stage's
+//     "full" mbarrier.
+//   * warps 2..5 (128 threads, thread = weight row): decode.  Each thread
+//     reads its row's 32 packed bytes, dequantises them in registers (the
+//     routine of wq_common.cuh; bf16 RNE of the exact weight) and writes the
+//     64 bf16 weights into TMEM with one tcgen05.st (32 columns of its lane).
+//     The weights never pass through shared memory.
+//   * warp 1, one lane: issues 4 x tcgen05.mma.kind::f16 (M=128, N=256, K=16)
+//     per k-step with A from TMEM, B from shared memory, the fp32
+//     accumulator in TMEM; tcgen05.commit frees the stage and the TMEM weight
+//     buffer.
+//   * warps 2..5 again: epilogue, tcgen05.ld of the accumulator (their lane
+//     quarter), fp32 -> bf16/fp32, stores to C.
+// Every wait is bounded in wall time (%globaltimer); a wait that runs out
+// records WQ_ERR_DEVICE_TIMEOUT in the device status word, the CTA unwinds
+// (outstanding TMA copies and MMAs are waited for, again with a bound) and
+// frees its tensor memory.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
 #include "wq_common.cuh"
 #include "wq_internal.h"
+#include "wq_tc.cuh"
 
 namespace wq {
 
@@ -17,9 +48,412 @@ int read_and_clear_device_status() {
     return v;
 }
 
-int launch_tc(const void*, const uint8_t*, const void*, const uint8_t*, void*, int, int, int, int, int, bool,
-              cudaStream_t) {
-    return WQ_ERR_UNSUPPORTED;
+namespace {
+
+using namespace sm100;
+
+constexpr int kBN = 128;        // weight rows per tile (MMA M)
+constexpr int kBM = 256;        // activation rows per tile (MMA N)
+constexpr int kBK = 64;         // k per stage
+constexpr int kStages = 4;
+constexpr int kWBufs = 4;       // TMEM weight buffers
+constexpr int kAccCols = kBM;   // fp32 accumulator columns
+constexpr int kWCols = kBK;     // TMEM columns per weight buffer: bf16 pairs, hi then lo (int4)
+constexpr int kTmemCols = 512;
+constexpr int kThreads = 192;
+constexpr int kATileBytes = kBM * kBK * 2;          // 32 KB
+constexpr int kPTileBytes = kBN * kBK / 2;          // 4 KB
+constexpr int kStageBytes = kATileBytes + kPTileBytes;
+constexpr uint32_t kIdesc = idesc_bf16_f32(kBN, kBM);
+constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s
+constexpr uint64_t kDrainNs = 100000000ull;        // 0.1 s
+
+static_assert(kAccCols + kWBufs * kWCols <= kTmemCols, "TMEM budget");
+static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned for the 128-byte swizzle");
+
+struct TcArgs {
+    const uint8_t* scales;
+    const uint8_t* zeros;
+    void* C;
+    int M, N, K, group;
+    int out_f32;
+};
+
+struct __align__(8) TcShared {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t wfull[kWBufs];
+    uint64_t wempty[kWBufs];
+    uint64_t accfull;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ void record_timeout() { atomicExch(&g_device_status, WQ_ERR_DEVICE_TIMEOUT); }
+
+// raw scale data of one row for one k-step (64 k):
+//   nvfp4: the 4 e4m3 bytes of groups 4ks..4ks+3
+//   mxfp4: the 2 e8m0 bytes of groups 2ks, 2ks+1
+//   int4 : (bf16 scale | zero << 16) of the groups of k = 64ks and 64ks + 32
+template <int FMT>
+__device__ __forceinline__ uint2 tc_raw(const TcArgs& a, int n, int ks) {
+    const int gpr = a.K / a.group;
+    uint2 r;
+    if constexpr (FMT == kNVFP4) {
+        const uint8_t* p = a.scales + (size_t)n * gpr + 4 * ks;
+        r.x = ldg_u8(p) | (ldg_u8(p + 1) << 8) | (ldg_u8(p + 2) << 16) | (ldg_u8(p + 3) << 24);
+        r.y = 0;
+    } else if constexpr (FMT == kMXFP4) {
+        const uint8_t* p = a.scales + (size_t)n * gpr + 2 * ks;
+        r.x = ldg_u8(p) | (ldg_u8(p + 1) << 8);
+        r.y = 0;
+    } else {
+        const int g0 = (ks * kBK) / a.group, g1 = (ks * kBK + 32) / a.group;
+        const uint16_t* s = reinterpret_cast<const uint16_t*>(a.scales) + (size_t)n * gpr;
+        const uint8_t* z = a.zeros + (size_t)n * gpr;
+        r.x = ldg_u16(s + g0) | (ldg_u8(z + g0) << 16);
+        r.y = ldg_u16(s + g1) | (ldg_u8(z + g1) << 16);
+    }
+    return r;
+}
+
+// the decode key of word i (codes k = 8i .. 8i+7 of the k-step)
+template <int FMT>
+__device__ __forceinline__ void tc_keys(uint2 raw, GroupKey (&key)[4]) {
+    if constexpr (FMT == kNVFP4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) key[j] = key_nvfp4((raw.x >> (8 * j)) & 0xFF);   // words 2j, 2j+1
+    } else if constexpr (FMT == kMXFP4) {
+        key[0] = key_mxfp4(raw.x & 0xFF);            // words 0..3
+        key[1] = key_mxfp4((raw.x >> 8) & 0xFF);     // words 4..7
+        key[2] = key[0];
+        key[3] = key[1];
+    } else {
+        key[0] = key_int4(raw.x & 0xFFFF, raw.x >> 16);
+        key[1] = key_int4(raw.y & 0xFFFF, raw.y >> 16);
+        key[2] = key[0];
+        key[3] = key[1];
+    }
+}
+
+template <int FMT>
+__device__ __forceinline__ const GroupKey& key_of_word(const GroupKey (&key)[4], int i) {
+    if constexpr (FMT == kNVFP4) return key[i >> 1];
+    else return key[i >> 2];
+}
+
+// One row's 64 weights of a k-step as bf16 pairs.  fp4 weights are exact in
+// bf16 (at most 6 significant bits); int4 weights come as the exact split
+// hi + lo (w2 = lo), so the tensor cores see the exact weight.
+template <int FMT, bool TWO>
+__device__ __forceinline__ void decode_row(const uint4& c0, const uint4& c1, const GroupKey (&key)[4],
+                                           uint32_t (&w)[32], uint32_t (&w2)[32]) {
+    const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t p[4], r[4];
+        if constexpr (FMT == kINT4) {
+            int4_word_split<TWO>(wd[i], key_of_word<FMT>(key, i), p, r);
+        } else {
+            word_scaled<FMT, TWO>(wd[i], key_of_word<FMT>(key, i), p);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            w[4 * i + e] = p[e];
+            if constexpr (FMT == kINT4) w2[4 * i + e] = r[e];
+        }
+    }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_kernel(const __grid_constant__ CUtensorMap tmapA, const __grid_constant__ CUtensorMap tmapP, const TcArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // stages 1024-byte aligned (the 128-byte swizzle pattern repeats every 1 KB)
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    TcShared& sh = *reinterpret_cast<TcShared*>(smem + kStages * kStageBytes);
+    volatile int* abort = &sh.abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * kBM;
+    const int nks = a.K / kBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&sh.full[s]), 1);
+            mbar_init(smem_u32(&sh.empty[s]), 1);
+        }
+        for (int b = 0; b < kWBufs; ++b) {
+            mbar_init(smem_u32(&sh.wfull[b]), 128);
+            mbar_init(smem_u32(&sh.wempty[b]), 1);
+        }
+        mbar_init(smem_u32(&sh.accfull), 1);
+        mbar_init(smem_u32(&sh.drain), 1);
+        sh.abort = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&sh.tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            prefetch_tensormap(&tmapA);
+            prefetch_tensormap(&tmapP);
+            int issued = 0;
+            for (int ks = 0; ks < nks; ++ks) {
+                const int s = ks % kStages;
+                const uint32_t ph = (ks / kStages) & 1;
+                if (!mbar_wait_bounded(smem_u32(&sh.empty[s]), ph ^ 1, abort, kWaitNs)) {
+                    record_timeout();
+                    break;
+                }
+                uint8_t* st = smem + s * kStageBytes;
+                const uint32_t fb = smem_u32(&sh.full[s]);
+                mbar_arrive_expect_tx(fb, kStageBytes);
+                tma_load_2d(smem_u32(st), &tmapA, fb, ks * kBK, m0);
+                tma_load_2d(smem_u32(st + kATileBytes), &tmapP, fb, ks * (kBK / 2), n0);
+                issued = ks + 1;
+            }
+            // never leave the CTA with copies in flight
+            for (int ks = (issued > kStages ? issued - kStages : 0); ks < issued; ++ks)
+                mbar_wait_timeout(smem_u32(&sh.full[ks % kStages]), (ks / kStages) & 1, kDrainNs);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            for (int ks = 0; ks < nks; ++ks) {
+                const int s = ks % kStages, b = ks % kWBufs;
+                const uint32_t ph = (ks / kStages) & 1, phb = (ks / kWBufs) & 1;
+                if (!mbar_wait_bounded(smem_u32(&sh.full[s]), ph, abort, kWaitNs) ||
+                    !mbar_wait_bounded(smem_u32(&sh.wfull[b]), phb, abort, kWaitNs)) {
+                    record_timeout();
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(smem + s * kStageBytes);
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    const uint64_t bdesc = smem_desc_sw128_kmajor(a_addr + kk * 32);
+                    const uint32_t wcol = tmem + kAccCols + b * kWCols + kk * 8;
+                    mma_ts_f16(tmem, wcol, bdesc, kIdesc, (ks | kk) != 0);
+                    if constexpr (FMT == kINT4) mma_ts_f16(tmem, wcol + 32, bdesc, kIdesc, 1);   // the residual
+                }
+                tc_commit(smem_u32(&sh.empty[s]));
+                tc_commit(smem_u32(&sh.wempty[b]));
+            }
+            tc_commit(smem_u32(&sh.accfull));
+            // every MMA of this thread has completed before the CTA tears down
+            tc_commit(smem_u32(&sh.drain));
+            mbar_wait_timeout(smem_u32(&sh.drain), 0, kDrainNs);
+        }
+    } else {
+        // ---------------- decode, then epilogue (warps 2..5) ----------------
+        const int q = warp & 3;                 // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;          // weight row inside the tile
+        const int n = n0 + row;
+        const int nc = n < a.N ? n : a.N - 1;   // rows past N decode row N-1 (never stored)
+        const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+        constexpr int D = 4;                    // k-steps of scales in flight
+        uint2 raw[D];
+#pragma unroll
+        for (int d = 0; d < D; ++d)
+            if (d < nks) raw[d] = tc_raw<FMT>(a, nc, d);
+        bool ok = true;
+        for (int ks0 = 0; ks0 < nks && ok; ks0 += D) {
+#pragma unroll
+            for (int d = 0; d < D; ++d) {
+                const int ks = ks0 + d;
+                if (ks < nks && ok) {
+                    const int s = ks % kStages, b = ks % kWBufs;
+                    const uint32_t ph = (ks / kStages) & 1, phb = (ks / kWBufs) & 1;
+                    GroupKey key[4];
+                    tc_keys<FMT>(raw[d], key);
+                    if (ks + D < nks) raw[d] = tc_raw<FMT>(a, nc, ks + D);
+                    const bool got = mbar_wait_bounded(smem_u32(&sh.full[s]), ph, abort, kWaitNs) &&
+                                     mbar_wait_bounded(smem_u32(&sh.wempty[b]), phb ^ 1, abort, kWaitNs);
+                    // the tcgen05.st below is warp-collective: decide as a warp
+                    if (!__all_sync(0xffffffffu, got)) {
+                        if (!got) record_timeout();
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // this row's 32 packed bytes; 32-byte swizzle: chunk c of row r
+                    // sits at 32 r + 16 (c ^ ((r >> 2) & 1))
+                    const uint8_t* prow = smem + s * kStageBytes + kATileBytes + row * 32;
+                    const int x = (row >> 2) & 1;
+                    const uint4 lo = *reinterpret_cast<const uint4*>(prow + 16 * x);
+                    const uint4 hi = *reinterpret_cast<const uint4*>(prow + 16 * (x ^ 1));
+                    uint32_t w[32], w2[32];
+                    bool two = false;
+                    if constexpr (FMT != kNVFP4) two = __any_sync(0xffffffffu, key[0].two || key[1].two);
+                    if (two) decode_row<FMT, true>(lo, hi, key, w, w2);
+                    else decode_row<FMT, false>(lo, hi, key, w, w2);
+                    tmem_st_32x32b_x32(lane_base + kAccCols + b * kWCols, w);
+                    if constexpr (FMT == kINT4) tmem_st_32x32b_x32(lane_base + kAccCols + b * kWCols + 32, w2);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&sh.wfull[b]));
+                }
+            }
+        }
+        // ---------------- epilogue ----------------
+        const bool acc_ready = ok && mbar_wait_bounded(smem_u32(&sh.accfull), 0, abort, kWaitNs);
+        if (__all_sync(0xffffffffu, acc_ready)) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int ch = 0; ch < kBM / 32; ++ch) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(lane_base + ch * 32, v);
+                tmem_wait_ld();
+                if (n < a.N) {
+                    const int mb = m0 + ch * 32;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (mb + j < a.M) {
+                            const size_t o = (size_t)(mb + j) * a.N + n;
+                            const float f = __uint_as_float(v[j]);
+                            if (a.out_f32) static_cast<float*>(a.C)[o] = f;
+                            else static_cast<__nv_bfloat16*>(a.C)[o] = __float2bfloat16_rn(f);
+                        }
+                    }
+                }
+            }
+        } else if (ok && !acc_ready) {
+            record_timeout();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side: tensor maps through the driver entry point (no libcuda link)
+// ---------------------------------------------------------------------------
+// WQ_DEBUG=1 in the environment prints why a call was refused
+bool debug_on() {
+    static const bool on = getenv("WQ_DEBUG") != nullptr;
+    return on;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        const cudaError_t e =
+            cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (e == cudaSuccess && q == cudaDriverEntryPointSuccess) fn = reinterpret_cast<EncodeTiledFn>(p);
+        else if (debug_on())
+            fprintf(stderr, "wq: driver entry point lookup failed (%s, %d)\n", cudaGetErrorString(e), (int)q);
+    });
+    return fn;
+}
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        if (debug_on()) fprintf(stderr, "wq: cuTensorMapEncodeTiled entry point not found\n");
+        return false;
+    }
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS && debug_on())
+        fprintf(stderr, "wq: cuTensorMapEncodeTiled failed (%d): dims %llu x %llu, stride %llu, box %u x %u\n",
+                (int)r, (unsigned long long)inner, (unsigned long long)outer, (unsigned long long)row_bytes,
+                box_inner, box_outer);
+    return r == CUDA_SUCCESS;
+}
+
+template <int FMT>
+int launch_fmt(const CUtensorMap& ta, const CUtensorMap& tp, const TcArgs& args, dim3 grid, size_t smem,
+               cudaStream_t stream) {
+    auto kern = tc_kernel<FMT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return WQ_ERR_CUDA;
+    kern<<<grid, kThreads, smem, stream>>>(ta, tp, args);
+    return cudaGetLastError() == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+}
+
+// Failure-path self test: one thread waits, with a short wall-time bound, on
+// an mbarrier that nothing will ever arrive on, then records the timeout the
+// way the GEMM kernels do.  No GPU is hung and the context stays usable.
+__global__ void timeout_selftest_kernel(unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbarrier_init();
+        if (!mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, limit_ns)) record_timeout();
+    }
+}
+
+}  // namespace
+
+int launch_timeout_selftest(cudaStream_t stream) {
+    timeout_selftest_kernel<<<1, 32, 0, stream>>>(20000000ull);   // 20 ms
+    return cudaGetLastError() == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+}
+
+int launch_tc(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C, int M,
+              int N, int K, int fmt, int group, bool out_f32, cudaStream_t stream) {
+    if (M == 0 || N == 0) return WQ_OK;
+    // shapes this kernel takes: whole k-steps, TMA-legal strides, aligned
+    // scale rows for the per-k-step scale loads
+    if (K <= 0 || K % kBK != 0) return WQ_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(packed) & 15))
+        return WQ_ERR_UNSUPPORTED;
+    if ((M + kBM - 1) / kBM > 65535) return WQ_ERR_UNSUPPORTED;
+
+    CUtensorMap ta, tp;
+    if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kBK, kBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+        return WQ_ERR_UNSUPPORTED;
+    if (!encode_2d(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2,
+                   kBK / 2, kBN, CU_TENSOR_MAP_SWIZZLE_32B))
+        return WQ_ERR_UNSUPPORTED;
+
+    TcArgs args;
+    args.scales = static_cast<const uint8_t*>(scales);
+    args.zeros = zeros;
+    args.C = C;
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.group = group;
+    args.out_f32 = out_f32 ? 1 : 0;
+    const dim3 grid((N + kBN - 1) / kBN, (M + kBM - 1) / kBM, 1);
+    const size_t smem = 1024 + (size_t)kStages * kStageBytes + sizeof(TcShared);
+    switch (fmt) {
+        case kNVFP4: return launch_fmt<kNVFP4>(ta, tp, args, grid, smem, stream);
+        case kMXFP4: return launch_fmt<kMXFP4>(ta, tp, args, grid, smem, stream);
+        default: return launch_fmt<kINT4>(ta, tp, args, grid, smem, stream);
+    }
 }
 
 }  // namespace wq

@@ -71,6 +71,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Wait with a wall-time bound only (no abort check): used when a CTA unwinds
+// and must still see its own copies / MMAs complete before it exits.
+__device__ __forceinline__ bool mbar_wait_timeout(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 31) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (tensor map in kernel-parameter space, no multicast)
 // ---------------------------------------------------------------------------

@@ -132,6 +132,27 @@ __device__ __forceinline__ uint32_t nvfp4_mul_bits(uint32_t b) {
     return ((230u + lz) << 7) | ((m << (7 - lz)) & 0x7Fu);
 }
 
+// Two NVFP4 multipliers at once, without branches: the hardware e4m3x2 ->
+// f16x2 conversion is exact (every e4m3 value, subnormals included, is a
+// normal f16 number or zero), and a normal f16 pattern h maps to the bf16
+// pattern of |value| * 2^112 as ((h & 0x7FFF) >> 3) + (224 << 7): the f16
+// exponent field rebased (-15 + 127 + 112) and the mantissa's top 7 bits,
+// which hold all 3 e4m3 mantissa bits.  Zero stays zero; NaN stays NaN.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+    uint32_t d;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+        : "=r"(d) : "r"(two_bytes));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t nvfp4_mul_from_f16(uint32_t h16) {
+    const uint32_t m = h16 & 0x7FFFu;
+    const uint32_t b = (m >> 3) + (224u << 7);
+    return m ? b : 0u;
+}
+
 __device__ __forceinline__ GroupKey key_nvfp4(uint32_t sbyte) {
     GroupKey k;
     k.mul = splat16(nvfp4_mul_bits(sbyte));

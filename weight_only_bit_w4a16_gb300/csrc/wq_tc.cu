@@ -2,25 +2,29 @@
 // the dequantised weights in tensor memory, and the device status word that
 // its bounded waits report into.
 //
-// Tile: 128 weight rows (n) x 256 activation rows (m) x all of K, in k-steps
-// of 64.  The product is computed transposed, D = W . A^T, so that the
-// dequantised weights are the A operand of tcgen05.mma and can live in TMEM:
+// Tile: 128 weight rows (n) x bm activation rows (m, a multiple of 32 up to
+// 256, chosen per call to limit the last partial wave) x all of K, in
+// k-steps of 64.  The product is computed transposed, D = W . A^T, so that
+// the dequantised weights are the A operand of tcgen05.mma and can live in
+// TMEM:
 //   * warp 0, one lane: TMA producer.  Per k-step it loads the activation
-//     tile (256 x 64 bf16, 128-byte swizzle, the MMA's B operand in shared
+//     tile (bm x 64 bf16, 128-byte swizzle, the MMA's B operand in shared
 //     memory) and the packed weight tile (128 rows x 32 bytes, 32-byte
 //     swizzle) into a ring of kStages stages, completing on the stage's
 //     "full" mbarrier.
-//   * warps 2..5 (128 threads, thread = weight row): decode.  Each thread
-//     reads its row's 32 packed bytes, dequantises them in registers (the
-//     routine of wq_common.cuh; bf16 RNE of the exact weight) and writes the
-//     64 bf16 weights into TMEM with one tcgen05.st (32 columns of its lane).
-//     The weights never pass through shared memory.
-//   * warp 1, one lane: issues 4 x tcgen05.mma.kind::f16 (M=128, N=256, K=16)
-//     per k-step with A from TMEM, B from shared memory, the fp32
-//     accumulator in TMEM; tcgen05.commit frees the stage and the TMEM weight
-//     buffer.
-//   * warps 2..5 again: epilogue, tcgen05.ld of the accumulator (their lane
-//     quarter), fp32 -> bf16/fp32, stores to C.
+//   * warps 2.. (kDecodeSets sets of 4 warps, thread = weight row; set j
+//     takes the k-steps ks = j mod kDecodeSets): decode.  Each thread reads
+//     its row's 32 packed bytes, dequantises them in registers (the routine
+//     of wq_common.cuh) and writes the 64 bf16 weights into TMEM with one
+//     tcgen05.st (32 columns of its lane); int4 weights go in as the exact
+//     two-term split hi + lo, two stores.  The weights never pass through
+//     shared memory.
+//   * warp 1, one lane: issues 4 (int4: 8) tcgen05.mma.kind::f16 (M=128,
+//     N=bm, K=16) per k-step with A from TMEM, B from shared memory, the
+//     fp32 accumulator in TMEM; tcgen05.commit frees the stage and the TMEM
+//     weight buffer.
+//   * the decode warps again: epilogue, tcgen05.ld of the accumulator (their
+//     lane quarter; the sets split the columns), fp32 -> bf16/fp32, stores.
 // Every wait is bounded in wall time (%globaltimer); a wait that runs out
 // records WQ_ERR_DEVICE_TIMEOUT in the device status word, the CTA unwinds
 // (outstanding TMA copies and MMAs are waited for, again with a bound) and
@@ -53,23 +57,20 @@ namespace {
 using namespace sm100;
 
 constexpr int kBN = 128;        // weight rows per tile (MMA M)
-constexpr int kBM = 256;        // activation rows per tile (MMA N)
+constexpr int kBMMax = 256;     // activation rows per tile (MMA N): a multiple of 32, <= 256
 constexpr int kBK = 64;         // k per stage
 constexpr int kStages = 4;
 constexpr int kWBufs = 4;       // TMEM weight buffers
-constexpr int kAccCols = kBM;   // fp32 accumulator columns
+constexpr int kAccCols = kBMMax;  // TMEM columns reserved for the fp32 accumulator
 constexpr int kWCols = kBK;     // TMEM columns per weight buffer: bf16 pairs, hi then lo (int4)
 constexpr int kTmemCols = 512;
-constexpr int kThreads = 192;
-constexpr int kATileBytes = kBM * kBK * 2;          // 32 KB
-constexpr int kPTileBytes = kBN * kBK / 2;          // 4 KB
-constexpr int kStageBytes = kATileBytes + kPTileBytes;
-constexpr uint32_t kIdesc = idesc_bf16_f32(kBN, kBM);
+constexpr int kDecodeSets = 2;                      // decode warp sets, alternating k-steps
+constexpr int kThreads = 64 + kDecodeSets * 128;    // producer, MMA, decode/epilogue warps
+constexpr int kPTileBytes = kBN * kBK / 2;          // 4 KB of packed weights per stage
 constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s
 constexpr uint64_t kDrainNs = 100000000ull;        // 0.1 s
 
 static_assert(kAccCols + kWBufs * kWCols <= kTmemCols, "TMEM budget");
-static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned for the 128-byte swizzle");
 
 struct TcArgs {
     const uint8_t* scales;
@@ -77,6 +78,10 @@ struct TcArgs {
     void* C;
     int M, N, K, group;
     int out_f32;
+    int bm;             // activation rows per tile (MMA N), a multiple of 32
+    int a_tile_bytes;   // bm * 128: the activation tile of a stage
+    int stage_bytes;    // a_tile_bytes + packed tile; a multiple of 1024 (128-byte swizzle period)
+    uint32_t idesc;     // instruction descriptor: M = 128, N = bm
 };
 
 struct __align__(8) TcShared {
@@ -122,8 +127,16 @@ __device__ __forceinline__ uint2 tc_raw(const TcArgs& a, int n, int ks) {
 template <int FMT>
 __device__ __forceinline__ void tc_keys(uint2 raw, GroupKey (&key)[4]) {
     if constexpr (FMT == kNVFP4) {
+        const uint32_t h01 = e4m3x2_to_f16x2(raw.x & 0xFFFF), h23 = e4m3x2_to_f16x2(raw.x >> 16);
+        const uint32_t hv[4] = {h01 & 0xFFFF, h01 >> 16, h23 & 0xFFFF, h23 >> 16};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) key[j] = key_nvfp4((raw.x >> (8 * j)) & 0xFF);   // words 2j, 2j+1
+        for (int j = 0; j < 4; ++j) {                 // words 2j, 2j+1
+            key[j].mul = splat16(nvfp4_mul_from_f16(hv[j]));
+            key[j].mul2 = 0x3F803F80u;
+            key[j].zz = 0;
+            key[j].zz2 = 0;
+            key[j].two = false;
+        }
     } else if constexpr (FMT == kMXFP4) {
         key[0] = key_mxfp4(raw.x & 0xFF);            // words 0..3
         key[1] = key_mxfp4((raw.x >> 8) & 0xFF);     // words 4..7
@@ -172,11 +185,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // stages 1024-byte aligned (the 128-byte swizzle pattern repeats every 1 KB)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int kStageBytes = a.stage_bytes, kATileBytes = a.a_tile_bytes;
     TcShared& sh = *reinterpret_cast<TcShared*>(smem + kStages * kStageBytes);
     volatile int* abort = &sh.abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * kBM;
+    const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * a.bm;
     const int nks = a.K / kBK;
 
     if (threadIdx.x == 0) {
@@ -243,8 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < kBK / 16; ++kk) {
                     const uint64_t bdesc = smem_desc_sw128_kmajor(a_addr + kk * 32);
                     const uint32_t wcol = tmem + kAccCols + b * kWCols + kk * 8;
-                    mma_ts_f16(tmem, wcol, bdesc, kIdesc, (ks | kk) != 0);
-                    if constexpr (FMT == kINT4) mma_ts_f16(tmem, wcol + 32, bdesc, kIdesc, 1);   // the residual
+                    mma_ts_f16(tmem, wcol, bdesc, a.idesc, (ks | kk) != 0);
+                    if constexpr (FMT == kINT4) mma_ts_f16(tmem, wcol + 32, bdesc, a.idesc, 1);   // the residual
                 }
                 tc_commit(smem_u32(&sh.empty[s]));
                 tc_commit(smem_u32(&sh.wempty[b]));
@@ -255,28 +269,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_timeout(smem_u32(&sh.drain), 0, kDrainNs);
         }
     } else {
-        // ---------------- decode, then epilogue (warps 2..5) ----------------
+        // ---------------- decode, then epilogue (warps 2..) ----------------
+        // set `dset` decodes the k-steps ks = dset (mod kDecodeSets); each
+        // set has one warp per TMEM lane quarter
+        const int dset = (warp - 2) >> 2;
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;          // weight row inside the tile
         const int n = n0 + row;
         const int nc = n < a.N ? n : a.N - 1;   // rows past N decode row N-1 (never stored)
         const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-        constexpr int D = 4;                    // k-steps of scales in flight
+        constexpr int D = 4;                    // this set's k-steps of scales in flight
+        constexpr int KS = kDecodeSets;
         uint2 raw[D];
 #pragma unroll
         for (int d = 0; d < D; ++d)
-            if (d < nks) raw[d] = tc_raw<FMT>(a, nc, d);
+            if (dset + d * KS < nks) raw[d] = tc_raw<FMT>(a, nc, dset + d * KS);
         bool ok = true;
-        for (int ks0 = 0; ks0 < nks && ok; ks0 += D) {
+        for (int ks0 = dset; ks0 < nks && ok; ks0 += D * KS) {
 #pragma unroll
             for (int d = 0; d < D; ++d) {
-                const int ks = ks0 + d;
+                const int ks = ks0 + d * KS;
                 if (ks < nks && ok) {
                     const int s = ks % kStages, b = ks % kWBufs;
                     const uint32_t ph = (ks / kStages) & 1, phb = (ks / kWBufs) & 1;
                     GroupKey key[4];
                     tc_keys<FMT>(raw[d], key);
-                    if (ks + D < nks) raw[d] = tc_raw<FMT>(a, nc, ks + D);
+                    if (ks + D * KS < nks) raw[d] = tc_raw<FMT>(a, nc, ks + D * KS);
                     const bool got = mbar_wait_bounded(smem_u32(&sh.full[s]), ph, abort, kWaitNs) &&
                                      mbar_wait_bounded(smem_u32(&sh.wempty[b]), phb ^ 1, abort, kWaitNs);
                     // the tcgen05.st below is warp-collective: decide as a warp
@@ -310,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__all_sync(0xffffffffu, acc_ready)) {
             tc_fence_after();
 #pragma unroll 1
-            for (int ch = 0; ch < kBM / 32; ++ch) {
+            for (int ch = dset; ch < a.bm / 32; ch += kDecodeSets) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(lane_base + ch * 32, v);
                 tmem_wait_ld();
@@ -428,10 +446,31 @@ int launch_tc(const void* A, const uint8_t* packed, const void* scales, const ui
     if (K <= 0 || K % kBK != 0) return WQ_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(packed) & 15))
         return WQ_ERR_UNSUPPORTED;
-    if ((M + kBM - 1) / kBM > 65535) return WQ_ERR_UNSUPPORTED;
+    int sms = 148, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // tile height: fewest waves of one-CTA-per-SM tiles, each costing about
+    // (bm + 64) -- MMA time grows with bm, the decode of a k-step does not
+    const int nt = (N + kBN - 1) / kBN;
+    int bm = 0;
+    long long best = -1;
+    for (int cand = kBMMax; cand >= 32; cand -= 32) {
+        if (cand < 128 && cand < ((M + 31) / 32) * 32) continue;   // small tiles only to fit a small M
+        const long long tiles = (long long)nt * ((M + cand - 1) / cand);
+        const long long cost = ((tiles + sms - 1) / sms) * (cand + 64);
+        if (best < 0 || cost < best) {
+            best = cost;
+            bm = cand;
+        }
+    }
+    if (const char* e = getenv("WQ_TC_BM")) {
+        const int v = atoi(e);
+        if (v >= 32 && v <= kBMMax && v % 32 == 0) bm = v;
+    }
+    if ((M + bm - 1) / bm > 65535) return WQ_ERR_UNSUPPORTED;
 
     CUtensorMap ta, tp;
-    if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kBK, kBM,
+    if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kBK, bm,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return WQ_ERR_UNSUPPORTED;
     if (!encode_2d(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2,
@@ -447,8 +486,12 @@ int launch_tc(const void* A, const uint8_t* packed, const void* scales, const ui
     args.K = K;
     args.group = group;
     args.out_f32 = out_f32 ? 1 : 0;
-    const dim3 grid((N + kBN - 1) / kBN, (M + kBM - 1) / kBM, 1);
-    const size_t smem = 1024 + (size_t)kStages * kStageBytes + sizeof(TcShared);
+    args.bm = bm;
+    args.a_tile_bytes = bm * kBK * 2;
+    args.stage_bytes = args.a_tile_bytes + kPTileBytes;
+    args.idesc = idesc_bf16_f32(kBN, bm);
+    const dim3 grid(nt, (M + bm - 1) / bm, 1);
+    const size_t smem = 1024 + (size_t)kStages * args.stage_bytes + sizeof(TcShared);
     switch (fmt) {
         case kNVFP4: return launch_fmt<kNVFP4>(ta, tp, args, grid, smem, stream);
         case kMXFP4: return launch_fmt<kMXFP4>(ta, tp, args, grid, smem, stream);

@@ -229,8 +229,49 @@ def test_cluster_kernel_variant(M, monkeypatch):
 
 @pytest.mark.parametrize("wk", ["0", "1", "2", "3", "4"])
 def test_split_kernel_warp_splits(wk, monkeypatch):
-    """Every K split of the in-CTA split kernel gives the same parity."""
+    """Every K split of the register-streaming split kernel gives the same parity."""
+    monkeypatch.setenv("WQ_GEMV_KERNEL", "split")
     monkeypatch.setenv("WQ_GEMV_WK_LOG2", wk)
     for fmt, M in (("int4", 1), ("int4", 12), ("mxfp4", 3)):
         p = synth.make_problem(fmt, M, 300, 3072, seed=int(wk) + M)
         check_full(p, "fp32", path="gemv", what=f"{fmt} wk={wk} M={M}")
+
+
+@pytest.mark.parametrize("rb,wk", [("1", "0"), ("1", "2"), ("1", "3"), ("2", "1"), ("2", "3"), ("4", "0"),
+                                   ("4", "2"), ("8", "1")])
+def test_streaming_kernel_cta_shapes(rb, wk, monkeypatch):
+    """Every CTA shape of the TMA-streaming GEMV (16-row blocks per CTA x warps
+    splitting K) gives the same parity, on ragged N and K and on every mode."""
+    monkeypatch.setenv("WQ_GEMV_RB", rb)
+    monkeypatch.setenv("WQ_GEMV_TMA_WK", wk)
+    cases = (("int4", 1, 300, 3072, 128), ("int4", 12, 200, 1024, 128), ("int4", 5, 70, 640, 64),
+             ("nvfp4", 3, 130, 544, 16), ("mxfp4", 16, 100, 2080, 32))
+    for fmt, M, N, K, g in cases:
+        p = synth.make_problem(fmt, M, N, K, group=g, seed=int(rb) * 10 + int(wk) + M)
+        check_full(p, "fp32", path="gemv", what=f"{fmt} rb={rb} wk={wk} M={M} N={N} K={K}")
+
+
+# -- the second exact decode step: int4 zero points above 128, MXFP4 E > 142 --
+@pytest.mark.parametrize("path", ["gemv", "auto"])
+@pytest.mark.parametrize("M", [3, 16, 96])
+@pytest.mark.parametrize("group", [128, 64])
+def test_int4_zero_points_above_128(path, M, group):
+    p = synth.make_problem("int4", M, 144, 1024, group=group, seed=M + group)
+    rng = np.random.default_rng(M)
+    z = p["zeros"].copy()
+    big = rng.random(z.shape) < 0.3
+    z[big] = rng.integers(129, 256, size=int(big.sum()), dtype=np.uint8)
+    p["zeros"] = z
+    check_full(p, "fp32", path=path, what=f"int4 big zeros g{group} M={M} {path}")
+
+
+@pytest.mark.parametrize("path", ["gemv", "auto"])
+@pytest.mark.parametrize("M", [3, 16, 96])
+def test_mxfp4_scales_above_2_pow_15(path, M):
+    p = synth.make_problem("mxfp4", M, 144, 1024, seed=M)
+    rng = np.random.default_rng(M)
+    E = p["scales"].copy()
+    big = rng.random(E.shape) < 0.3
+    E[big] = rng.integers(143, 161, size=int(big.sum()), dtype=np.uint8)
+    p["scales"] = E
+    check_full(p, "fp32", path=path, what=f"mxfp4 E>142 M={M} {path}")

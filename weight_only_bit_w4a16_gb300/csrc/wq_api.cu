@@ -78,7 +78,11 @@ WQ_EXPORT int wq_dequant(const uint8_t* packed, const void* scales, const uint8_
     return wq::launch_dequant(packed, scales, zeros, W, N, K, format, group, static_cast<cudaStream_t>(stream));
 }
 
-WQ_EXPORT int wq_get_device_error(void) { return wq::read_and_clear_device_status(); }
+WQ_EXPORT int wq_get_device_error(void) {
+    const int a = wq::read_and_clear_device_status();
+    const int b = wq::read_and_clear_gemv_status();
+    return a != 0 ? a : b;
+}
 
 WQ_EXPORT int wq_selftest_timeout(void* stream) {
     return wq::launch_timeout_selftest(static_cast<cudaStream_t>(stream));

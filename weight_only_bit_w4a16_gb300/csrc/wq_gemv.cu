@@ -29,8 +29,9 @@
 //     order -- deterministic, with no global workspace and no atomics.
 #include <cooperative_groups.h>
 #include <cstdlib>
+#include <cstring>
 
-#include "wq_common.cuh"
+#include "wq_gemv.cuh"
 #include "wq_internal.h"
 
 namespace cg = cooperative_groups;
@@ -39,11 +40,9 @@ namespace wq {
 
 namespace {
 
-constexpr int kItK = 128;   // k per warp-iteration
-constexpr int kPF = 4;      // iterations of packed data in flight per lane
+using namespace gemv;
 
-constexpr int kModeInt4 = 0;     // int4 with group 128: exact (code - zero), scale after the MMA
-constexpr int kModeScaled = 1;   // every other case: weights scaled before the MMA
+constexpr int kPF = 4;      // iterations of packed data in flight per lane
 
 struct GemvArgs {
     const uint16_t* A;
@@ -58,32 +57,6 @@ struct GemvArgs {
     int row_blocks;    // split kernel: 16-row blocks per CTA
     int wk_log2;       // split kernel: log2 of the warps that split K for one row block
 };
-
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// 16-byte unit u of activation row m, swizzled inside aligned groups of 16
-// units: the 8 lanes of a quarter-warp (2 rows x 4 chunk lanes) land on 8
-// different bank groups.
-__device__ __forceinline__ int a_unit(int u, int m) { return u ^ ((((u >> 3) & 1) << 1) | (m & 1)); }
-
-// programmatic dependent launch: no-ops when the grid was launched without it
-__device__ __forceinline__ void grid_dependents_launch() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
-    uint4 v;
-    asm("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr));
-    return v;
-}
 
 // Scale / zero-point sources of one row: its scale bytes and zero points.
 struct RowScales {
@@ -137,118 +110,6 @@ __device__ __forceinline__ void fetch(const GemvArgs& a, const uint8_t* prow, co
     const bool ok = g * kItK + c * 32 < a.K;
     q = ldg_stream_v4(prow + (ok ? (size_t)g * 64 + c * 16 : 0));
     raw = load_raw<FMT, MODE>(a, rs, g, c, ok);
-}
-
-template <int FMT>
-__device__ __forceinline__ void keys_of(uint32_t raw, GroupKey& k0, GroupKey& k1) {
-    if constexpr (FMT == kNVFP4) {
-        k0 = key_nvfp4(raw & 0xFF);
-        k1 = key_nvfp4((raw >> 8) & 0xFF);
-    } else if constexpr (FMT == kMXFP4) {
-        k0 = key_mxfp4(raw & 0xFF);
-        k1 = k0;
-    } else {
-        k0 = key_int4(raw & 0xFFFF, raw >> 16);
-        k1 = k0;
-    }
-}
-
-// int4 codes of one word minus the zero point, as exact bf16 integers, in
-// the (k, k+4) pair order: (k0,k4), (k1,k5), (k2,k6), (k3,k7).  The
-// exponent-bias trick makes bf16(128 + code) with one mask-and-or, and one
-// exact bf16x2 subtraction of (128 + zero) leaves (code - zero).  Zero points
-// above 128 take a second exact subtraction (TWO).
-// (x & 0x000F000F) | magic as one lop3 with the magic in a register
-__device__ __forceinline__ uint32_t nib_or_magic(uint32_t x, uint32_t magic) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(d) : "r"(x), "r"(magic));
-    return d;
-}
-
-template <bool TWO>
-__device__ __forceinline__ void int4_word_kk4(uint32_t w, uint32_t zz, uint32_t zz2, uint32_t (&p)[4]) {
-    const uint32_t magic = 0x43004300u;
-    p[0] = bf16x2_sub(nib_or_magic(w, magic), zz);
-    p[1] = bf16x2_sub(nib_or_magic(w >> 4, magic), zz);
-    p[2] = bf16x2_sub(nib_or_magic(w >> 8, magic), zz);
-    p[3] = bf16x2_sub(nib_or_magic(w >> 12, magic), zz);
-    if constexpr (TWO) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) p[i] = bf16x2_sub(p[i], zz2);
-    }
-}
-
-// bf16x2 subtrahends of a zero point: (128 + z) for z <= 128 (0x4300 + z is
-// exactly 128 + z, the carry of z = 128 moving into the exponent), else 128
-// and then z itself
-// Branch-free: zz = 128 + min(z, 128) (exact; 0x4300 + z is 128 + z, the
-// carry of z = 128 moving into the exponent), zz2 = z - min(z, 128) as a bf16
-// integer (0..127: exact, its float bits truncate to bf16 without rounding).
-__device__ __forceinline__ void zero_subtrahends(uint32_t z, uint32_t& zz, uint32_t& zz2) {
-    const uint32_t zc = min(z, 128u);
-    zz = 0x43004300u + zc * 0x10001u;
-    const float d = __uint_as_float(0x4B000000u | (z - zc)) - 8388608.0f;
-    zz2 = (__float_as_uint(d) >> 16) * 0x10001u;
-}
-
-// One iteration (16 rows x 128 k) of the int4 group-128 path: the MMAs run on
-// the exact integers (code - zero); the group's scale multiplies the fp32
-// partial sums afterwards ("subtract before multiply").  Two accumulation
-// chains shorten the dependent MMA sequence.
-template <int NT, bool TWO>
-__device__ __forceinline__ void iteration_int4(const uint4& qa, const uint4& qb, const uint32_t (&abase)[NT][4],
-                                               int ioff, float (&acc)[NT][4], uint32_t zzA,
-                                               uint32_t zzA2, uint32_t zzB, uint32_t zzB2, float sa, float sb) {
-    const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
-    const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
-    float part[2][NT][4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int t = 0; t < NT; ++t)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) part[h][t][e] = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint32_t pa[4], pb[4];
-        int4_word_kk4<TWO>(wa[j], zzA, zzA2, pa);
-        int4_word_kk4<TWO>(wb[j], zzB, zzB2, pb);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            const uint4 bv = lds128(abase[t][j] + ioff);
-            mma16816(part[j & 1][t], pa[0], pb[0], pa[1], pb[1], bv.x, bv.y);
-            mma16816(part[j & 1][t], pa[2], pb[2], pa[3], pb[3], bv.z, bv.w);
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-        acc[t][0] = fmaf(sa, part[0][t][0] + part[1][t][0], acc[t][0]);
-        acc[t][1] = fmaf(sa, part[0][t][1] + part[1][t][1], acc[t][1]);
-        acc[t][2] = fmaf(sb, part[0][t][2] + part[1][t][2], acc[t][2]);
-        acc[t][3] = fmaf(sb, part[0][t][3] + part[1][t][3], acc[t][3]);
-    }
-}
-
-// One iteration of the generic path: weights decoded with their scale (bf16
-// RNE of the exact weight) in natural pair order, then the MMAs.
-template <int FMT, int NT, bool TWO>
-__device__ __forceinline__ void iteration_scaled(const uint4& qa, const uint4& qb, const GroupKey (&ka)[2],
-                                                 const GroupKey (&kb)[2], const uint32_t (&abase)[NT][4],
-                                                 int ioff, float (&acc)[NT][4]) {
-    const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
-    const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint32_t pa[4], pb[4];
-        word_scaled<FMT, TWO>(wa[j], ka[j >> 1], pa);
-        word_scaled<FMT, TWO>(wb[j], kb[j >> 1], pb);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            const uint4 bv = lds128(abase[t][j] + ioff);
-            mma16816(acc[t], pa[0], pb[0], pa[1], pb[1], bv.x, bv.y);
-            mma16816(acc[t], pa[2], pb[2], pa[3], pb[3], bv.z, bv.w);
-        }
-    }
 }
 
 template <int FMT, int NT, int MODE>
@@ -680,6 +541,14 @@ int launch_inst(const GemvArgs& args, dim3 grid, int threads, size_t smem, int c
 int launch_gemv(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C,
                 int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, cudaStream_t stream) {
     if (M == 0 || N == 0) return WQ_OK;
+    // WQ_GEMV_KERNEL=split|cluster (tests, tuning) skips the streaming kernel
+    const char* force = getenv("WQ_GEMV_KERNEL");
+    const bool force_cluster = getenv("WQ_GEMV_FORCE_CLUSTER") || (force && !strcmp(force, "cluster"));
+    const bool force_split = force && !strcmp(force, "split");
+    if (!force_cluster && !force_split) {
+        const int st = launch_gemv_tma(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, pdl, stream);
+        if (st != WQ_ERR_UNSUPPORTED) return st;
+    }
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -719,7 +588,7 @@ int launch_gemv(const void* A, const uint8_t* packed, const void* scales, const 
     }
     const int Wk = 1 << wk_log2;
     const size_t smem_split = (size_t)Mc * total_its * kItK * 2 + (size_t)R * 16 * Wk * MP * sizeof(float);
-    const bool split_kernel = smem_split <= 112 * 1024 && !getenv("WQ_GEMV_FORCE_CLUSTER");
+    const bool split_kernel = smem_split <= 112 * 1024 && !force_cluster;
 
     dim3 grid;
     int threads, cluster_x = 1;

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/wq.h"
@@ -17,6 +18,12 @@ int launch_dequant(const uint8_t* packed, const void* scales, const uint8_t* zer
 int launch_gemv(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
                 void* C, int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, cudaStream_t stream);
 
+// The streaming small-M kernel (all of a CTA's weights requested by TMA up
+// front).  Returns WQ_ERR_UNSUPPORTED (without launching) for shapes it does
+// not take; launch_gemv then uses the register-streaming kernels.
+int launch_gemv_tma(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
+                    void* C, int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, cudaStream_t stream);
+
 // Returns WQ_ERR_UNSUPPORTED (without launching) for shapes the tensor-core
 // kernel does not take.
 int launch_tc(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
@@ -25,7 +32,17 @@ int launch_tc(const void* A, const uint8_t* packed, const void* scales, const ui
 // A kernel whose bounded wait is bound to run out (tests the failure path).
 int launch_timeout_selftest(cudaStream_t stream);
 
-// Device status word of the current device: read and clear.
+// Device status words of the current device (one per kernel module): read
+// and clear; the first non-zero one wins.
 int read_and_clear_device_status();
+int read_and_clear_gemv_status();
+
+// WQ_DEBUG=1 in the environment prints why a call was refused.
+bool debug_on();
+
+// 2D tiled tensor map (row-major, `inner` elements per row, `outer` rows,
+// rows `row_bytes` apart) through the driver entry point, no libcuda link.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
 
 }  // namespace wq

@@ -358,6 +358,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+template <int FMT>
+int launch_fmt(const CUtensorMap& ta, const CUtensorMap& tp, const TcArgs& args, dim3 grid, size_t smem,
+               cudaStream_t stream) {
+    auto kern = tc_kernel<FMT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return WQ_ERR_CUDA;
+    kern<<<grid, kThreads, smem, stream>>>(ta, tp, args);
+    return cudaGetLastError() == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+}
+
+// Failure-path self test: one thread waits, with a short wall-time bound, on
+// an mbarrier that nothing will ever arrive on, then records the timeout the
+// way the GEMM kernels do.  No GPU is hung and the context stays usable.
+__global__ void timeout_selftest_kernel(unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbarrier_init();
+        if (!mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, limit_ns)) record_timeout();
+    }
+}
+
+}  // namespace
+
 // ---------------------------------------------------------------------------
 // host side: tensor maps through the driver entry point (no libcuda link)
 // ---------------------------------------------------------------------------
@@ -371,7 +397,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn encode_fn() {
+static EncodeTiledFn encode_fn() {
     static EncodeTiledFn fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -406,32 +432,6 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
                 box_inner, box_outer);
     return r == CUDA_SUCCESS;
 }
-
-template <int FMT>
-int launch_fmt(const CUtensorMap& ta, const CUtensorMap& tp, const TcArgs& args, dim3 grid, size_t smem,
-               cudaStream_t stream) {
-    auto kern = tc_kernel<FMT>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return WQ_ERR_CUDA;
-    kern<<<grid, kThreads, smem, stream>>>(ta, tp, args);
-    return cudaGetLastError() == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
-}
-
-// Failure-path self test: one thread waits, with a short wall-time bound, on
-// an mbarrier that nothing will ever arrive on, then records the timeout the
-// way the GEMM kernels do.  No GPU is hung and the context stays usable.
-__global__ void timeout_selftest_kernel(unsigned long long limit_ns) {
-    __shared__ __align__(8) uint64_t bar;
-    __shared__ int abort_flag;
-    if (threadIdx.x == 0) {
-        abort_flag = 0;
-        mbar_init(smem_u32(&bar), 1);
-        fence_mbarrier_init();
-        if (!mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, limit_ns)) record_timeout();
-    }
-}
-
-}  // namespace
 
 int launch_timeout_selftest(cudaStream_t stream) {
     timeout_selftest_kernel<<<1, 32, 0, stream>>>(20000000ull);   // 20 ms

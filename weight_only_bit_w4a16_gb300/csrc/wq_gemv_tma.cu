@@ -389,8 +389,10 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const TmaGemvArgs a
     }
     two = __any_sync(0xffffffffu, two);
 
-    // the next kernel on the stream may start (programmatic dependent launch);
-    // A is read, and C written, only after the preceding kernel has finished
+    // the next kernel on the stream may start (programmatic dependent launch:
+    // triggered once this CTA's own weight requests are out, so the next
+    // call's stream follows this one's instead of competing with it); A is
+    // read, and C written, only after the preceding kernel has finished
     grid_dependents_launch();
     grid_dependency_wait();
 
@@ -582,8 +584,9 @@ bool choose_plan(KernFn kern, int fmt, int mode, int NT, int Mc, int mchunks, in
                 double cost = per_sm * rb * n_its * c_it / 4.0 + per_sm * (double)Mc * n_its * kItK * 2 / 48.0 +
                               p.ipw * c_it + (waves - 1) * 2500.0 + (pad ? 0.0 : 300.0);
                 // chained launches stream the next call's weights while this one
-                // computes only if a second CTA fits beside this kernel's own
-                if (pdl && occ < per_sm + 1) cost += 4000.0;
+                // computes only if the next kernel's CTAs fit beside this
+                // kernel's own: room for a second generation on every SM
+                if (pdl && occ < 2 * per_sm) cost += 4000.0;
                 if (best_cost < 0 || cost < best_cost) {
                     best_cost = cost;
                     best = p;

@@ -103,6 +103,35 @@ int wq_gemm_ex(const void* A, const uint8_t* packed, const void* scales, const u
                void* C, int M, int N, int K, int format, int group, void* stream, int path);
 
 /*
+ * wq_gemm_ws -- wq_gemm_ex with a caller-owned device workspace that the
+ * tensor-core path may use to balance its tiles over the SMs ("stream-K": a
+ * tile whose k-steps are shared by two or more CTAs is finished by the CTA
+ * holding its last k-step, which adds the fp32 partial sums the others left
+ * in the workspace, in a fixed CTA order -- deterministic, no atomics on C).
+ * The paper pages have no counterpart; it is a load-balancing device of this
+ * library and computes the same sum of products as wq_gemm_ex.
+ *   workspace        256-byte aligned device memory (NULL with 0 bytes: the
+ *                    call behaves as wq_gemm_ex).  It must hold zeros before
+ *                    its first use (cudaMemset); every completed call leaves
+ *                    it zero again, so one workspace serves any number of
+ *                    calls that are ordered on the device (one stream).
+ *                    After a call that reported WQ_ERR_DEVICE_TIMEOUT it must
+ *                    be zeroed again.
+ *   workspace_bytes  its size; below wq_gemm_workspace_size() for this shape
+ *                    the tiles run whole, as in wq_gemm_ex.
+ * Returns WQ_ERR_ALIGN for a misaligned workspace, WQ_ERR_INVALID_ARG for a
+ * NULL workspace with a non-zero size.
+ */
+int wq_gemm_ws(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
+               void* C, int M, int N, int K, int format, int group, void* workspace,
+               size_t workspace_bytes, void* stream, int path);
+
+/* Workspace bytes wq_gemm_ws can use for this shape on the current device
+ * (0: the shape needs none -- M <= 16, tiles that fill whole waves, or an
+ * invalid description). */
+size_t wq_gemm_workspace_size(int M, int N, int K, int format, int group);
+
+/*
  * wq_dequant -- W = deq(packed, scales, zeros) as an (N, K) row-major bf16
  * matrix, each weight rounded to nearest even from its exact value (so the
  * result equals the oracle's bf16 image bit for bit; NaN stays NaN, overflow

@@ -31,9 +31,9 @@ def to_dev(p, dev=None):
     return A, packed, scales, zeros
 
 
-def gpu_gemm(p, out="bf16", path="auto"):
+def gpu_gemm(p, out="bf16", path="auto", workspace=None):
     A, packed, scales, zeros = to_dev(p)
-    C = wq.gemm(A, packed, scales, zeros, p["fmt"], p["group"], out_dtype=out, path=path)
+    C = wq.gemm(A, packed, scales, zeros, p["fmt"], p["group"], out_dtype=out, path=path, workspace=workspace)
     torch.cuda.synchronize()
     assert wq.wq_get_device_error() == wq.WQ_OK
     return C.float().cpu().numpy().astype(np.float64)
@@ -68,17 +68,17 @@ def assert_parity(C, Ce, S, out, what=""):
             f"gpu={C[i]!r} exact={Ce[i]!r} tol={tol[i]!r}")
 
 
-def check_full(p, out, path="auto", what=""):
-    C = gpu_gemm(p, out, path)
+def check_full(p, out, path="auto", what="", workspace=None):
+    C = gpu_gemm(p, out, path, workspace)
     Ce, S = oracle_ref(p)
     assert_parity(C, Ce, S, out, what)
     return C
 
 
-def check_sampled(p, out, path="auto", k=24, seed=0, what=""):
+def check_sampled(p, out, path="auto", k=24, seed=0, what="", workspace=None):
     """Full GPU result; oracle on sampled rows (all columns) and sampled
     columns (all rows)."""
-    C = gpu_gemm(p, out, path)
+    C = gpu_gemm(p, out, path, workspace)
     M, N = C.shape
     rows = sample(M, k, seed)
     cols = sample(N, k, seed + 1)

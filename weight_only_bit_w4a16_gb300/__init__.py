@@ -41,6 +41,8 @@ _vp, _i = ctypes.c_void_p, ctypes.c_int
 SIGNATURES = {
     "wq_gemm": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i]),
     "wq_gemm_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i]),
+    "wq_gemm_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, ctypes.c_size_t, _vp, _i]),
+    "wq_gemm_workspace_size": (ctypes.c_size_t, [_i, _i, _i, _i, _i]),
     "wq_dequant": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "wq_get_device_error": (_i, []),
     "wq_selftest_timeout": (_i, [_vp]),
@@ -84,6 +86,16 @@ def wq_gemm(A, packed, scales, zeros, C, M, N, K, format, group) -> int:
 
 def wq_gemm_ex(A, packed, scales, zeros, C, M, N, K, format, group, stream, path) -> int:
     return lib().wq_gemm_ex(A, packed, scales, zeros, C, M, N, K, format, group, stream, path)
+
+
+def wq_gemm_ws(A, packed, scales, zeros, C, M, N, K, format, group, workspace, workspace_bytes, stream,
+               path) -> int:
+    return lib().wq_gemm_ws(A, packed, scales, zeros, C, M, N, K, format, group, workspace, workspace_bytes,
+                            stream, path)
+
+
+def wq_gemm_workspace_size(M, N, K, format, group) -> int:
+    return lib().wq_gemm_workspace_size(M, N, K, format, group)
 
 
 def wq_dequant(packed, scales, zeros, W, N, K, format, group, stream) -> int:
@@ -134,13 +146,36 @@ def _stream_handle(stream, device):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+_workspaces = {}
+
+
+def workspace(M, N, K, fmt, group=None, device=None):
+    """A zeroed device workspace for wq_gemm_ws on this shape (None if the
+    shape needs none), cached per device and grown as needed.  Completed calls
+    leave it zero, so it is reused across calls on one stream."""
+    import torch
+    group = group or DEFAULT_GROUP[_fmt_name(fmt)]
+    nbytes = wq_gemm_workspace_size(M, N, K, _fmt(fmt), int(group))
+    if nbytes == 0:
+        return None
+    dev = torch.device(device if device is not None else "cuda")
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=torch.device("cuda", key))
+        _workspaces[key] = ws
+    return ws
+
+
 def gemm(A, packed, scales, zeros, fmt, group=None, out_dtype="bf16", out=None, path="auto", stream=None,
-         overlap=False):
+         overlap=False, workspace=None):
     """C = A . deq(packed, scales, zeros)^T on A's device and current stream.
 
     overlap=True sets WQ_LAUNCH_OVERLAP (programmatic dependent launch): the
     caller guarantees the preceding kernel on the stream does not write the
-    weights.
+    weights.  workspace: a zeroed uint8 CUDA tensor (see workspace()) that
+    lets the tensor-core path split tiles over the SMs; "auto" takes the
+    cached one.
 
     A: (M, K) bf16; packed: (N, K/2) uint8; scales: (N, K/group) uint8
     (nvfp4 e4m3 / mxfp4 e8m0 bytes) or bf16 (int4); zeros: (N, K/group)
@@ -165,10 +200,18 @@ def gemm(A, packed, scales, zeros, fmt, group=None, out_dtype="bf16", out=None, 
         raise ValueError("out has the wrong shape or dtype")
     fmt_word = f | (WQ_OUT_F32 if odt == torch.float32 else 0)
     pcode = (PATHS[path] if isinstance(path, str) else int(path)) | (WQ_LAUNCH_OVERLAP if overlap else 0)
-    st = wq_gemm_ex(_ptr(A), _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(out), M, N, K, fmt_word,
-                    int(group), _stream_handle(stream, A.device), pcode)
+    if isinstance(workspace, str) and workspace == "auto":
+        workspace = globals()["workspace"](M, N, K, fmt, group, A.device)
+    if workspace is None:
+        st = wq_gemm_ex(_ptr(A), _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(out), M, N, K, fmt_word,
+                        int(group), _stream_handle(stream, A.device), pcode)
+    else:
+        if not workspace.is_cuda or workspace.dtype != torch.uint8:
+            raise ValueError("workspace must be a uint8 CUDA tensor")
+        st = wq_gemm_ws(_ptr(A), _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(out), M, N, K, fmt_word,
+                        int(group), _ptr(workspace), workspace.numel(), _stream_handle(stream, A.device), pcode)
     if st != WQ_OK:
-        raise WQError(st, "wq_gemm_ex")
+        raise WQError(st, "wq_gemm")
     return out
 
 

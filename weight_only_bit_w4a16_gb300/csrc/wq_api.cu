@@ -33,10 +33,11 @@ int check_weights(const uint8_t* packed, const void* scales, const uint8_t* zero
 
 #define WQ_EXPORT __attribute__((visibility("default")))
 
-extern "C" {
+namespace {
 
-WQ_EXPORT int wq_gemm_ex(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C,
-               int M, int N, int K, int format, int group, void* stream, int path) {
+int gemm_impl(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C, int M,
+              int N, int K, int format, int group, void* workspace, size_t workspace_bytes, void* stream,
+              int path) {
     if (format & ~(0xFF | WQ_OUT_F32)) return WQ_ERR_INVALID_ARG;
     const int fmt = format & 0xFF;
     const bool out_f32 = (format & WQ_OUT_F32) != 0;
@@ -45,21 +46,49 @@ WQ_EXPORT int wq_gemm_ex(const void* A, const uint8_t* packed, const void* scale
     const bool overlap = (path & WQ_LAUNCH_OVERLAP) != 0;
     path &= 0xFF;
     if (path != WQ_PATH_AUTO && path != WQ_PATH_GEMV && path != WQ_PATH_TC) return WQ_ERR_INVALID_ARG;
+    if (workspace_bytes > 0 && !workspace) return WQ_ERR_INVALID_ARG;
+    if (workspace && !aligned(workspace, 256)) return WQ_ERR_ALIGN;
     int st = check_weights(packed, scales, zeros, N, K, fmt, group);
     if (st != WQ_OK) return st;
     if (M == 0 || N == 0) return WQ_OK;
     if (!C || (K > 0 && !A)) return WQ_ERR_INVALID_ARG;
     if (!aligned(C, 16) || (K > 0 && !aligned(A, 16))) return WQ_ERR_ALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (workspace_bytes == 0) workspace = nullptr;
 
     if (path == WQ_PATH_TC)
-        return wq::launch_tc(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, s);
+        return wq::launch_tc(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, workspace, workspace_bytes,
+                             s);
     if (path == WQ_PATH_AUTO && M > 16 && K > 0) {
-        st = wq::launch_tc(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, s);
+        st = wq::launch_tc(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, workspace, workspace_bytes, s);
         if (st != WQ_ERR_UNSUPPORTED) return st;
         // shapes the tensor-core kernel does not take run on the GEMV kernel
     }
     return wq::launch_gemv(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, overlap, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+WQ_EXPORT int wq_gemm_ex(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C,
+               int M, int N, int K, int format, int group, void* stream, int path) {
+    return gemm_impl(A, packed, scales, zeros, C, M, N, K, format, group, nullptr, 0, stream, path);
+}
+
+WQ_EXPORT int wq_gemm_ws(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C,
+               int M, int N, int K, int format, int group, void* workspace, size_t workspace_bytes, void* stream,
+               int path) {
+    return gemm_impl(A, packed, scales, zeros, C, M, N, K, format, group, workspace, workspace_bytes, stream, path);
+}
+
+WQ_EXPORT size_t wq_gemm_workspace_size(int M, int N, int K, int format, int group) {
+    if (M <= 16 || N <= 0 || K <= 0) return 0;
+    if (check_weights(reinterpret_cast<const uint8_t*>(16), reinterpret_cast<const void*>(16),
+                      (format & 0xFF) == WQ_INT4 ? reinterpret_cast<const uint8_t*>(16) : nullptr, N, K,
+                      format & 0xFF, group) != WQ_OK)
+        return 0;
+    return wq::tc_workspace_bytes(M, N, K);
 }
 
 WQ_EXPORT int wq_gemm(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C, int M,

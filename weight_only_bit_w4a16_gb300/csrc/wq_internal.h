@@ -25,9 +25,14 @@ int launch_gemv_tma(const void* A, const uint8_t* packed, const void* scales, co
                     void* C, int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, cudaStream_t stream);
 
 // Returns WQ_ERR_UNSUPPORTED (without launching) for shapes the tensor-core
-// kernel does not take.
+// kernel does not take.  With a workspace of at least tc_workspace_bytes()
+// (zero-initialised before its first use; every completed call leaves it
+// zero) the kernel may split tiles across CTAs (stream-K); without one each
+// CTA computes whole tiles.
 int launch_tc(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
-              void* C, int M, int N, int K, int fmt, int group, bool out_f32, cudaStream_t stream);
+              void* C, int M, int N, int K, int fmt, int group, bool out_f32, void* workspace,
+              size_t workspace_bytes, cudaStream_t stream);
+size_t tc_workspace_bytes(int M, int N, int K);
 
 // A kernel whose bounded wait is bound to run out (tests the failure path).
 int launch_timeout_selftest(cudaStream_t stream);

@@ -76,12 +76,18 @@ struct TcArgs {
     const uint8_t* scales;
     const uint8_t* zeros;
     void* C;
+    float* ws;          // stream-K partial sums [G][bm / 32][8][128] float4; null: one tile per CTA
+    unsigned* flags;    // stream-K "partial of CTA c is ready" flags [G], zero between calls
     int M, N, K, group;
     int out_f32;
     int bm;             // activation rows per tile (MMA N), a multiple of 32
     int a_tile_bytes;   // bm * 128: the activation tile of a stage
     int stage_bytes;    // a_tile_bytes + packed tile; a multiple of 1024 (128-byte swizzle period)
     uint32_t idesc;     // instruction descriptor: M = 128, N = bm
+    int nt_n;           // tiles along N; tile t covers rows (t % nt_n) * 128, activations (t / nt_n) * bm
+    int nks;            // k-steps per tile
+    long long units;    // tiles * nks
+    int G;              // CTAs of a stream-K launch
 };
 
 struct __align__(8) TcShared {
@@ -90,6 +96,7 @@ struct __align__(8) TcShared {
     uint64_t wfull[kWBufs];
     uint64_t wempty[kWBufs];
     uint64_t accfull;
+    uint64_t accempty;
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -179,6 +186,77 @@ __device__ __forceinline__ void decode_row(const uint4& c0, const uint4& c1, con
     }
 }
 
+// ---------------------------------------------------------------------------
+// work split
+// ---------------------------------------------------------------------------
+// Data-parallel launch (no workspace): CTA c computes tile c, all k-steps.
+// Stream-K launch: the tiles * nks (tile, k-step) units are cut into G equal
+// contiguous ranges, one per CTA; a tile met by several CTAs is finished by
+// the CTA holding its last k-step (the owner), which adds the fp32 partial
+// sums the others left in the workspace, in increasing CTA order.
+__device__ __forceinline__ long long unit_start(const TcArgs& a, int c) {
+    return a.ws ? (long long)c * a.units / a.G : (long long)c * a.nks;
+}
+
+// CTA whose range holds unit u (stream-K)
+__device__ __forceinline__ int cta_of_unit(const TcArgs& a, long long u) {
+    int c = (int)((u * a.G) / a.units);
+    while (c + 1 < a.G && unit_start(a, c + 1) <= u) ++c;
+    while (c > 0 && unit_start(a, c) > u) --c;
+    return c;
+}
+
+// Segment i of CTA c in processing order: the last segment first when it
+// does not end its tile (its partial is then written before anyone waits on
+// it), then the tile-ending segments in order.  Every role of the CTA walks
+// the same sequence.  Returns false past the last segment.
+__device__ __forceinline__ bool get_seg(const TcArgs& a, int c, int i, int& tile, int& kb, int& ke) {
+    const long long u0 = unit_start(a, c), u1 = unit_start(a, c + 1);
+    if (u1 <= u0) return false;
+    const long long nks = a.nks;
+    const int t_first = (int)(u0 / nks), t_last = (int)((u1 - 1) / nks);
+    const bool last_partial = (u1 % nks) != 0;
+    if (last_partial) {
+        if (i == 0) {
+            tile = t_last;
+            kb = (int)((u0 > t_last * nks ? u0 : t_last * nks) - t_last * nks);
+            ke = (int)(u1 - t_last * nks);
+            return true;
+        }
+        --i;
+    }
+    const int t = t_first + i;
+    if (t > (last_partial ? t_last - 1 : t_last)) return false;
+    tile = t;
+    kb = (int)((u0 > t * nks ? u0 : t * nks) - t * nks);
+    ke = (int)nks;
+    return true;
+}
+
+// the fp32 partial of CTA `slot`: columns 32 ch + 4 j .. + 3 of row `row`,
+// laid out [slot][ch][j][row] in float4 so that a warp's 32 rows of one
+// (ch, j) are one contiguous 512-byte run
+__device__ __forceinline__ float4* partial_ptr(const TcArgs& a, int slot, int ch, int j, int row) {
+    return reinterpret_cast<float4*>(a.ws) + (((size_t)slot * (a.bm / 32) + ch) * 8 + j) * kBN + row;
+}
+
+__device__ __forceinline__ bool wait_flag(const unsigned* f, volatile int* abort, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0;; ++i) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+        if (v) return true;
+        if ((i & 15) == 15) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > limit_ns) {
+                *abort = 1;
+                return false;
+            }
+        }
+        __nanosleep(32);
+    }
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap tmapA, const __grid_constant__ CUtensorMap tmapP, const TcArgs a) {
@@ -190,8 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort = &sh.abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * a.bm;
-    const int nks = a.K / kBK;
+    const int cta = blockIdx.x;
+    const int nks = a.nks;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -203,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&sh.wempty[b]), 1);
         }
         mbar_init(smem_u32(&sh.accfull), 1);
+        mbar_init(smem_u32(&sh.accempty), kDecodeSets * 128);
         mbar_init(smem_u32(&sh.drain), 1);
         sh.abort = 0;
         fence_mbarrier_init();
@@ -221,132 +300,213 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             prefetch_tensormap(&tmapA);
             prefetch_tensormap(&tmapP);
-            int issued = 0;
-            for (int ks = 0; ks < nks; ++ks) {
-                const int s = ks % kStages;
-                const uint32_t ph = (ks / kStages) & 1;
-                if (!mbar_wait_bounded(smem_u32(&sh.empty[s]), ph ^ 1, abort, kWaitNs)) {
-                    record_timeout();
-                    break;
+            int g = 0;   // k-steps issued so far (the stage ring runs across segments)
+            bool ok = true;
+            int tile, kb, ke;
+            for (int i = 0; ok && get_seg(a, cta, i, tile, kb, ke); ++i) {
+                const int n0 = (tile % a.nt_n) * kBN, m0 = (tile / a.nt_n) * a.bm;
+                for (int k = kb; k < ke; ++k, ++g) {
+                    const int s = g % kStages;
+                    const uint32_t ph = (g / kStages) & 1;
+                    if (!mbar_wait_bounded(smem_u32(&sh.empty[s]), ph ^ 1, abort, kWaitNs)) {
+                        record_timeout();
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + s * kStageBytes;
+                    const uint32_t fb = smem_u32(&sh.full[s]);
+                    mbar_arrive_expect_tx(fb, kStageBytes);
+                    tma_load_2d(smem_u32(st), &tmapA, fb, k * kBK, m0);
+                    tma_load_2d(smem_u32(st + kATileBytes), &tmapP, fb, k * (kBK / 2), n0);
                 }
-                uint8_t* st = smem + s * kStageBytes;
-                const uint32_t fb = smem_u32(&sh.full[s]);
-                mbar_arrive_expect_tx(fb, kStageBytes);
-                tma_load_2d(smem_u32(st), &tmapA, fb, ks * kBK, m0);
-                tma_load_2d(smem_u32(st + kATileBytes), &tmapP, fb, ks * (kBK / 2), n0);
-                issued = ks + 1;
             }
             // never leave the CTA with copies in flight
-            for (int ks = (issued > kStages ? issued - kStages : 0); ks < issued; ++ks)
-                mbar_wait_timeout(smem_u32(&sh.full[ks % kStages]), (ks / kStages) & 1, kDrainNs);
+            for (int k = (g > kStages ? g - kStages : 0); k < g; ++k)
+                mbar_wait_timeout(smem_u32(&sh.full[k % kStages]), (k / kStages) & 1, kDrainNs);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            for (int ks = 0; ks < nks; ++ks) {
-                const int s = ks % kStages, b = ks % kWBufs;
-                const uint32_t ph = (ks / kStages) & 1, phb = (ks / kWBufs) & 1;
-                if (!mbar_wait_bounded(smem_u32(&sh.full[s]), ph, abort, kWaitNs) ||
-                    !mbar_wait_bounded(smem_u32(&sh.wfull[b]), phb, abort, kWaitNs)) {
+            int g = 0;
+            bool ok = true;
+            int tile, kb, ke;
+            for (int i = 0; ok && get_seg(a, cta, i, tile, kb, ke); ++i) {
+                // the epilogue of the previous segment has read the accumulator
+                if (i > 0 && !mbar_wait_bounded(smem_u32(&sh.accempty), (i - 1) & 1, abort, kWaitNs)) {
                     record_timeout();
                     break;
                 }
-                tc_fence_after();
-                const uint32_t a_addr = smem_u32(smem + s * kStageBytes);
+                for (int k = kb; k < ke; ++k, ++g) {
+                    const int s = g % kStages, b = g % kWBufs;
+                    const uint32_t ph = (g / kStages) & 1, phb = (g / kWBufs) & 1;
+                    if (!mbar_wait_bounded(smem_u32(&sh.full[s]), ph, abort, kWaitNs) ||
+                        !mbar_wait_bounded(smem_u32(&sh.wfull[b]), phb, abort, kWaitNs)) {
+                        record_timeout();
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + s * kStageBytes);
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {
-                    const uint64_t bdesc = smem_desc_sw128_kmajor(a_addr + kk * 32);
-                    const uint32_t wcol = tmem + kAccCols + b * kWCols + kk * 8;
-                    mma_ts_f16(tmem, wcol, bdesc, a.idesc, (ks | kk) != 0);
-                    if constexpr (FMT == kINT4) mma_ts_f16(tmem, wcol + 32, bdesc, a.idesc, 1);   // the residual
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t bdesc = smem_desc_sw128_kmajor(a_addr + kk * 32);
+                        const uint32_t wcol = tmem + kAccCols + b * kWCols + kk * 8;
+                        mma_ts_f16(tmem, wcol, bdesc, a.idesc, (k != kb || kk != 0) ? 1u : 0u);
+                        if constexpr (FMT == kINT4) mma_ts_f16(tmem, wcol + 32, bdesc, a.idesc, 1);   // the residual
+                    }
+                    tc_commit(smem_u32(&sh.empty[s]));
+                    tc_commit(smem_u32(&sh.wempty[b]));
                 }
-                tc_commit(smem_u32(&sh.empty[s]));
-                tc_commit(smem_u32(&sh.wempty[b]));
+                if (ok) tc_commit(smem_u32(&sh.accfull));
             }
-            tc_commit(smem_u32(&sh.accfull));
             // every MMA of this thread has completed before the CTA tears down
             tc_commit(smem_u32(&sh.drain));
             mbar_wait_timeout(smem_u32(&sh.drain), 0, kDrainNs);
         }
     } else {
         // ---------------- decode, then epilogue (warps 2..) ----------------
-        // set `dset` decodes the k-steps ks = dset (mod kDecodeSets); each
-        // set has one warp per TMEM lane quarter
+        // set `dset` decodes the k-steps g = dset (mod kDecodeSets) of the
+        // CTA's running k-step count; each set has one warp per TMEM lane
+        // quarter.  Failures do not leave the segment loop: every epilogue
+        // thread passes the same named barriers.
         const int dset = (warp - 2) >> 2;
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;          // weight row inside the tile
-        const int n = n0 + row;
-        const int nc = n < a.N ? n : a.N - 1;   // rows past N decode row N-1 (never stored)
         const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
         constexpr int D = 4;                    // this set's k-steps of scales in flight
         constexpr int KS = kDecodeSets;
-        uint2 raw[D];
-#pragma unroll
-        for (int d = 0; d < D; ++d)
-            if (dset + d * KS < nks) raw[d] = tc_raw<FMT>(a, nc, dset + d * KS);
+        int g = 0;
         bool ok = true;
-        for (int ks0 = dset; ks0 < nks && ok; ks0 += D * KS) {
+        int tile, kb, ke;
+        for (int i = 0; get_seg(a, cta, i, tile, kb, ke); ++i) {
+            const int n0 = (tile % a.nt_n) * kBN, m0 = (tile / a.nt_n) * a.bm;
+            const int n = n0 + row;
+            const int nc = n < a.N ? n : a.N - 1;   // rows past N decode row N-1 (never stored)
+            const int g0 = g;
+            const int k1 = kb + ((dset ^ g0) & 1);  // this set's first k-step of the segment
+            uint2 raw[D];
 #pragma unroll
-            for (int d = 0; d < D; ++d) {
-                const int ks = ks0 + d * KS;
-                if (ks < nks && ok) {
-                    const int s = ks % kStages, b = ks % kWBufs;
-                    const uint32_t ph = (ks / kStages) & 1, phb = (ks / kWBufs) & 1;
-                    GroupKey key[4];
-                    tc_keys<FMT>(raw[d], key);
-                    if (ks + D * KS < nks) raw[d] = tc_raw<FMT>(a, nc, ks + D * KS);
-                    const bool got = mbar_wait_bounded(smem_u32(&sh.full[s]), ph, abort, kWaitNs) &&
-                                     mbar_wait_bounded(smem_u32(&sh.wempty[b]), phb ^ 1, abort, kWaitNs);
-                    // the tcgen05.st below is warp-collective: decide as a warp
-                    if (!__all_sync(0xffffffffu, got)) {
-                        if (!got) record_timeout();
-                        ok = false;
-                        break;
+            for (int d = 0; d < D; ++d)
+                if (k1 + d * KS < ke) raw[d] = tc_raw<FMT>(a, nc, k1 + d * KS);
+            for (int kk0 = k1; kk0 < ke && ok; kk0 += D * KS) {
+#pragma unroll
+                for (int d = 0; d < D; ++d) {
+                    const int k = kk0 + d * KS;
+                    if (k < ke && ok) {
+                        const int gg = g0 + (k - kb);
+                        const int s = gg % kStages, b = gg % kWBufs;
+                        const uint32_t ph = (gg / kStages) & 1, phb = (gg / kWBufs) & 1;
+                        GroupKey key[4];
+                        tc_keys<FMT>(raw[d], key);
+                        if (k + D * KS < ke) raw[d] = tc_raw<FMT>(a, nc, k + D * KS);
+                        const bool got = mbar_wait_bounded(smem_u32(&sh.full[s]), ph, abort, kWaitNs) &&
+                                         mbar_wait_bounded(smem_u32(&sh.wempty[b]), phb ^ 1, abort, kWaitNs);
+                        // the tcgen05.st below is warp-collective: decide as a warp
+                        if (!__all_sync(0xffffffffu, got)) {
+                            if (!got) record_timeout();
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        // this row's 32 packed bytes; 32-byte swizzle: chunk c of row r
+                        // sits at 32 r + 16 (c ^ ((r >> 2) & 1))
+                        const uint8_t* prow = smem + s * kStageBytes + kATileBytes + row * 32;
+                        const int x = (row >> 2) & 1;
+                        const uint4 lo = *reinterpret_cast<const uint4*>(prow + 16 * x);
+                        const uint4 hi = *reinterpret_cast<const uint4*>(prow + 16 * (x ^ 1));
+                        uint32_t w[32], w2[32];
+                        bool two = false;
+                        if constexpr (FMT != kNVFP4) two = __any_sync(0xffffffffu, key[0].two || key[1].two);
+                        if (two) decode_row<FMT, true>(lo, hi, key, w, w2);
+                        else decode_row<FMT, false>(lo, hi, key, w, w2);
+                        tmem_st_32x32b_x32(lane_base + kAccCols + b * kWCols, w);
+                        if constexpr (FMT == kINT4) tmem_st_32x32b_x32(lane_base + kAccCols + b * kWCols + 32, w2);
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(smem_u32(&sh.wfull[b]));
                     }
-                    tc_fence_after();
-                    // this row's 32 packed bytes; 32-byte swizzle: chunk c of row r
-                    // sits at 32 r + 16 (c ^ ((r >> 2) & 1))
-                    const uint8_t* prow = smem + s * kStageBytes + kATileBytes + row * 32;
-                    const int x = (row >> 2) & 1;
-                    const uint4 lo = *reinterpret_cast<const uint4*>(prow + 16 * x);
-                    const uint4 hi = *reinterpret_cast<const uint4*>(prow + 16 * (x ^ 1));
-                    uint32_t w[32], w2[32];
-                    bool two = false;
-                    if constexpr (FMT != kNVFP4) two = __any_sync(0xffffffffu, key[0].two || key[1].two);
-                    if (two) decode_row<FMT, true>(lo, hi, key, w, w2);
-                    else decode_row<FMT, false>(lo, hi, key, w, w2);
-                    tmem_st_32x32b_x32(lane_base + kAccCols + b * kWCols, w);
-                    if constexpr (FMT == kINT4) tmem_st_32x32b_x32(lane_base + kAccCols + b * kWCols + 32, w2);
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(smem_u32(&sh.wfull[b]));
                 }
             }
-        }
-        // ---------------- epilogue ----------------
-        const bool acc_ready = ok && mbar_wait_bounded(smem_u32(&sh.accfull), 0, abort, kWaitNs);
-        if (__all_sync(0xffffffffu, acc_ready)) {
+            g = g0 + (ke - kb);
+
+            // ---------------- epilogue of the segment ----------------
+            const bool owner = ke == nks;
+            const int cfirst = (owner && a.ws) ? cta_of_unit(a, (long long)tile * nks) : cta;
+            if (ok) ok = mbar_wait_bounded(smem_u32(&sh.accfull), i & 1, abort, kWaitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok && owner) {
+                // the lanes poll the contributors' flags together (one memory
+                // round trip per pass, not per contributor)
+                for (int c0 = cfirst; c0 < cta && ok; c0 += 32) {
+                    const int c2 = c0 + lane;
+                    const bool mine = c2 < cta;
+                    const bool got = !mine || wait_flag(a.flags + c2, abort, kWaitNs);
+                    ok = __all_sync(0xffffffffu, got);
+                }
+            }
+            // the warp's reads of the partials below are ordered after the
+            // lanes' acquires of their flags
+            __syncwarp();
+            if (!ok && lane == 0) record_timeout();
             tc_fence_after();
 #pragma unroll 1
             for (int ch = dset; ch < a.bm / 32; ch += kDecodeSets) {
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(lane_base + ch * 32, v);
-                tmem_wait_ld();
+                if (ok) {
+                    tmem_ld_32x32b_x32(lane_base + ch * 32, v);
+                    tmem_wait_ld();
+                }
+                if (!ok) continue;
+                if (!owner) {
+                    // a tile this CTA starts but does not end: its partial sums
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        __stcg(partial_ptr(a, cta, ch, j, row), make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
+                    continue;
+                }
+                float f[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+                for (int c2 = cfirst; c2 < cta; ++c2) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 t = __ldcg(partial_ptr(a, c2, ch, j, row));
+                        f[4 * j] += t.x;
+                        f[4 * j + 1] += t.y;
+                        f[4 * j + 2] += t.z;
+                        f[4 * j + 3] += t.w;
+                    }
+                }
                 if (n < a.N) {
                     const int mb = m0 + ch * 32;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         if (mb + j < a.M) {
                             const size_t o = (size_t)(mb + j) * a.N + n;
-                            const float f = __uint_as_float(v[j]);
-                            if (a.out_f32) static_cast<float*>(a.C)[o] = f;
-                            else static_cast<__nv_bfloat16*>(a.C)[o] = __float2bfloat16_rn(f);
+                            if (a.out_f32) static_cast<float*>(a.C)[o] = f[j];
+                            else static_cast<__nv_bfloat16*>(a.C)[o] = __float2bfloat16_rn(f[j]);
                         }
                     }
                 }
             }
-        } else if (ok && !acc_ready) {
-            record_timeout();
+            // the accumulator may be overwritten by the next segment's MMAs
+            tc_fence_before();
+            mbar_arrive(smem_u32(&sh.accempty));
+            if (a.ws && (!owner || cfirst < cta)) {
+                // every epilogue thread is done with the partials it writes / reads
+                asm volatile("bar.sync 1, %0;" ::"n"(kDecodeSets * 128) : "memory");
+                if (warp == 2 && lane == 0 && ok) {
+                    if (!owner) {
+                        __threadfence();
+                        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a.flags + cta), "r"(1u) : "memory");
+                    } else {
+                        // consumed: leave the flags zero for the next call
+                        for (int c2 = cfirst; c2 < cta; ++c2)
+                            asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(a.flags + c2), "r"(0u) : "memory");
+                    }
+                }
+            }
         }
     }
 
@@ -438,26 +598,27 @@ int launch_timeout_selftest(cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
 }
 
-int launch_tc(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C, int M,
-              int N, int K, int fmt, int group, bool out_f32, cudaStream_t stream) {
-    if (M == 0 || N == 0) return WQ_OK;
-    // shapes this kernel takes: whole k-steps, TMA-legal strides, aligned
-    // scale rows for the per-k-step scale loads
-    if (K <= 0 || K % kBK != 0) return WQ_ERR_UNSUPPORTED;
-    if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(packed) & 15))
-        return WQ_ERR_UNSUPPORTED;
+namespace {
+
+int device_sms() {
     int sms = 148, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    // tile height: fewest waves of one-CTA-per-SM tiles, each costing about
-    // (bm + 64) -- MMA time grows with bm, the decode of a k-step does not
+    return sms;
+}
+
+// Tile height (MMA N) for M activation rows.  Data-parallel: fewest waves of
+// one-CTA-per-SM tiles, each costing about (bm + 64) -- MMA time grows with
+// bm, the decode of a k-step does not.  Stream-K: least total work,
+// tiles x (bm + 64), as the CTAs share it evenly.
+int choose_bm(int M, int N, int sms, bool streamk) {
     const int nt = (N + kBN - 1) / kBN;
     int bm = 0;
     long long best = -1;
     for (int cand = kBMMax; cand >= 32; cand -= 32) {
         if (cand < 128 && cand < ((M + 31) / 32) * 32) continue;   // small tiles only to fit a small M
         const long long tiles = (long long)nt * ((M + cand - 1) / cand);
-        const long long cost = ((tiles + sms - 1) / sms) * (cand + 64);
+        const long long cost = streamk ? tiles * (cand + 64) : ((tiles + sms - 1) / sms) * (cand + 64);
         if (best < 0 || cost < best) {
             best = cost;
             bm = cand;
@@ -467,7 +628,68 @@ int launch_tc(const void* A, const uint8_t* packed, const void* scales, const ui
         const int v = atoi(e);
         if (v >= 32 && v <= kBMMax && v % 32 == 0) bm = v;
     }
-    if ((M + bm - 1) / bm > 65535) return WQ_ERR_UNSUPPORTED;
+    return bm;
+}
+
+struct TcPlan {
+    int bm, nt_n, tiles, nks, G;
+    long long units;
+    bool streamk;
+    size_t ws_bytes;   // workspace a stream-K launch needs (0 if none)
+};
+
+constexpr size_t kFlagBytes(int G) { return ((size_t)G * sizeof(unsigned) + 255) / 256 * 256; }
+
+TcPlan plan_tc(int M, int N, int K, int sms, bool allow_streamk) {
+    TcPlan p{};
+    p.nks = K / kBK;
+    p.nt_n = (N + kBN - 1) / kBN;
+    // stream-K where whole tiles would leave the waves badly filled: below 75%
+    // the balance wins; above it the extra epilogue of a split tile (partials
+    // out, partials in) costs more than the idle SMs (measured: 2048 x 3072 x
+    // 3072 runs 87% full on whole tiles and is faster that way; 128 x 3072 x
+    // 3072 -- 24 tiles on 152 SMs -- runs 1.8x faster split)
+    int bm = choose_bm(M, N, sms, false);
+    long long tiles = (long long)p.nt_n * ((M + bm - 1) / bm);
+    const long long waves = (tiles + sms - 1) / sms;
+    bool sk = allow_streamk && (double)tiles / (double)(waves * sms) < 0.75;
+    if (allow_streamk && getenv("WQ_TC_STREAMK")) sk = atoi(getenv("WQ_TC_STREAMK")) != 0;   // tests, tuning
+    if (sk) {
+        bm = choose_bm(M, N, sms, true);
+        tiles = (long long)p.nt_n * ((M + bm - 1) / bm);
+    }
+    p.bm = bm;
+    p.tiles = (int)tiles;
+    p.units = tiles * p.nks;
+    p.streamk = sk;
+    p.G = sk ? (int)(p.units < sms ? p.units : sms) : (int)tiles;
+    // the flag words cover every CTA a launch on this device can have, so a
+    // later call with more CTAs never reads an earlier call's partials as flags
+    p.ws_bytes = sk ? kFlagBytes(sms) + (size_t)p.G * kBN * bm * sizeof(float) : 0;
+    return p;
+}
+
+}  // namespace
+
+size_t tc_workspace_bytes(int M, int N, int K) {
+    if (M <= 0 || N <= 0 || K <= 0 || K % kBK != 0) return 0;
+    return plan_tc(M, N, K, device_sms(), true).ws_bytes;
+}
+
+int launch_tc(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C, int M,
+              int N, int K, int fmt, int group, bool out_f32, void* workspace, size_t workspace_bytes,
+              cudaStream_t stream) {
+    if (M == 0 || N == 0) return WQ_OK;
+    // shapes this kernel takes: whole k-steps, TMA-legal strides, aligned
+    // scale rows for the per-k-step scale loads
+    if (K <= 0 || K % kBK != 0) return WQ_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(packed) & 15))
+        return WQ_ERR_UNSUPPORTED;
+    const int sms = device_sms();
+    TcPlan plan = plan_tc(M, N, K, sms, workspace != nullptr);
+    if (plan.streamk && workspace_bytes < plan.ws_bytes) plan = plan_tc(M, N, K, sms, false);
+    const int bm = plan.bm;
+    if (!plan.streamk && plan.tiles > 0x7FFFFFFF) return WQ_ERR_UNSUPPORTED;
 
     CUtensorMap ta, tp;
     if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kBK, bm,
@@ -481,6 +703,12 @@ int launch_tc(const void* A, const uint8_t* packed, const void* scales, const ui
     args.scales = static_cast<const uint8_t*>(scales);
     args.zeros = zeros;
     args.C = C;
+    args.ws = nullptr;
+    args.flags = nullptr;
+    if (plan.streamk) {
+        args.flags = static_cast<unsigned*>(workspace);
+        args.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kFlagBytes(sms));
+    }
     args.M = M;
     args.N = N;
     args.K = K;
@@ -490,7 +718,14 @@ int launch_tc(const void* A, const uint8_t* packed, const void* scales, const ui
     args.a_tile_bytes = bm * kBK * 2;
     args.stage_bytes = args.a_tile_bytes + kPTileBytes;
     args.idesc = idesc_bf16_f32(kBN, bm);
-    const dim3 grid(nt, (M + bm - 1) / bm, 1);
+    args.nt_n = plan.nt_n;
+    args.nks = plan.nks;
+    args.units = plan.units;
+    args.G = plan.G;
+    if (debug_on())
+        fprintf(stderr, "wq: tcgen05 M=%d N=%d K=%d: bm=%d tiles=%d %s grid=%d\n", M, N, K, bm, plan.tiles,
+                plan.streamk ? "stream-K" : "data-parallel", plan.G);
+    const dim3 grid(plan.G, 1, 1);
     const size_t smem = 1024 + (size_t)kStages * args.stage_bytes + sizeof(TcShared);
     switch (fmt) {
         case kNVFP4: return launch_fmt<kNVFP4>(ta, tp, args, grid, smem, stream);

@@ -126,6 +126,21 @@ int wq_gemm_ws(const void* A, const uint8_t* packed, const void* scales, const u
                void* C, int M, int N, int K, int format, int group, void* workspace,
                size_t workspace_bytes, void* stream, int path);
 
+/*
+ * wq_gemm_static -- wq_gemm_ws with the library's own scratch instead of a
+ * caller-owned workspace: a fixed device array inside the library (room for
+ * the split tiles of up to 160 SMs), found once per device, so the call
+ * allocates nothing.  The paper pages have no counterpart; it exists so that
+ * a caller without a memory allocator still gets the balanced tensor-core
+ * path.  Limits: one scratch per device, so calls through this entry point
+ * must be ordered on the device (one stream at a time), and a shape whose
+ * split would need more scratch than the array holds returns
+ * WQ_ERR_UNSUPPORTED without launching (WQ_STATIC_WS_CAP in the environment
+ * lowers the usable size, for tests).  Otherwise as wq_gemm_ex.
+ */
+int wq_gemm_static(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
+                   void* C, int M, int N, int K, int format, int group, void* stream, int path);
+
 /* Workspace bytes wq_gemm_ws can use for this shape on the current device
  * (0: the shape needs none -- M <= 16, tiles that fill whole waves, or an
  * invalid description). */

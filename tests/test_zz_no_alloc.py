@@ -1,0 +1,58 @@
+"""wq_gemm_static: the tensor-core path's tile splitting with the library's
+own scratch (a fixed device array found once per device) -- no allocation by
+the caller or the library.  Parity against the oracle, the scratch left
+usable across calls, and the refusal of a shape whose split would need more
+scratch than is there."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import weight_only_bit_w4a16_gb300 as wq
+from weight_only_bit_w4a16_gb300 import synth
+
+from gpu_util import assert_parity, oracle_ref, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run_static(p, out="fp32", path=wq.WQ_PATH_AUTO):
+    A, packed, scales, zeros = to_dev(p)
+    odt = torch.float32 if out == "fp32" else torch.bfloat16
+    C = torch.empty((p["M"], p["N"]), dtype=odt, device="cuda")
+    fmt = wq.FORMATS[p["fmt"]] | (wq.WQ_OUT_F32 if out == "fp32" else 0)
+    st = wq.wq_gemm_static(A.data_ptr(), packed.data_ptr(), scales.data_ptr(),
+                           zeros.data_ptr() if zeros is not None else None, C.data_ptr(),
+                           p["M"], p["N"], p["K"], fmt, p["group"],
+                           torch.cuda.current_stream().cuda_stream, path)
+    torch.cuda.synchronize()
+    return st, C.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("fmt,M,N,K", [("int4", 128, 3072, 3072), ("nvfp4", 17, 384, 4096),
+                                       ("mxfp4", 300, 1000, 1024), ("int4", 4, 512, 1024)])
+def test_static_scratch_parity(fmt, M, N, K):
+    p = synth.make_problem(fmt, M, N, K, seed=M + K)
+    # the split really happens for the tensor-core shapes
+    if M > 16:
+        assert wq.wq_gemm_workspace_size(M, N, K, wq.FORMATS[fmt], p["group"]) > 0
+    for rep in range(2):   # the second call finds the flags the first left zero
+        st, C = run_static(p)
+        assert st == wq.WQ_OK
+        assert wq.wq_get_device_error() == wq.WQ_OK
+        Ce, S = oracle_ref(p)
+        assert_parity(C, Ce, S, "fp32", f"static {fmt} {M}x{N}x{K} call {rep}")
+
+
+def test_static_scratch_refuses_oversize(monkeypatch):
+    p = synth.make_problem("int4", 128, 3072, 3072, seed=2)
+    need = wq.wq_gemm_workspace_size(128, 3072, 3072, wq.WQ_INT4, 128)
+    monkeypatch.setenv("WQ_STATIC_WS_CAP", str(need - 1))
+    st, _ = run_static(p)
+    assert st == wq.WQ_ERR_UNSUPPORTED
+    monkeypatch.setenv("WQ_STATIC_WS_CAP", str(need))
+    st, C = run_static(p)
+    assert st == wq.WQ_OK
+    Ce, S = oracle_ref(p)
+    assert_parity(C, Ce, S, "fp32", "static at exact capacity")

@@ -43,6 +43,7 @@ SIGNATURES = {
     "wq_gemm_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i]),
     "wq_gemm_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, ctypes.c_size_t, _vp, _i]),
     "wq_gemm_workspace_size": (ctypes.c_size_t, [_i, _i, _i, _i, _i]),
+    "wq_gemm_static": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i]),
     "wq_dequant": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "wq_get_device_error": (_i, []),
     "wq_selftest_timeout": (_i, [_vp]),
@@ -92,6 +93,10 @@ def wq_gemm_ws(A, packed, scales, zeros, C, M, N, K, format, group, workspace, w
                path) -> int:
     return lib().wq_gemm_ws(A, packed, scales, zeros, C, M, N, K, format, group, workspace, workspace_bytes,
                             stream, path)
+
+
+def wq_gemm_static(A, packed, scales, zeros, C, M, N, K, format, group, stream, path) -> int:
+    return lib().wq_gemm_static(A, packed, scales, zeros, C, M, N, K, format, group, stream, path)
 
 
 def wq_gemm_workspace_size(M, N, K, format, group) -> int:

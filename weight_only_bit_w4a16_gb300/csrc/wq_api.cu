@@ -2,6 +2,7 @@
 // selection.  Nothing here computes; every step of the product runs in the
 // kernels of wq_dequant.cu, wq_gemv.cu and wq_tc.cu.
 #include <cstdint>
+#include <cstdlib>
 
 #include "wq_internal.h"
 
@@ -80,6 +81,20 @@ WQ_EXPORT int wq_gemm_ws(const void* A, const uint8_t* packed, const void* scale
                int M, int N, int K, int format, int group, void* workspace, size_t workspace_bytes, void* stream,
                int path) {
     return gemm_impl(A, packed, scales, zeros, C, M, N, K, format, group, workspace, workspace_bytes, stream, path);
+}
+
+WQ_EXPORT int wq_gemm_static(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
+                             void* C, int M, int N, int K, int format, int group, void* stream, int path) {
+    size_t cap = 0;
+    void* ws = wq::static_workspace(&cap);
+    if (!ws) return WQ_ERR_CUDA;
+    if (const char* e = getenv("WQ_STATIC_WS_CAP")) {   // tests: a smaller usable part
+        const size_t v = (size_t)strtoull(e, nullptr, 10);
+        if (v < cap) cap = v;
+    }
+    const size_t need = (M > 16 && N > 0 && K > 0 && K % 64 == 0) ? wq::tc_workspace_bytes(M, N, K) : 0;
+    if (need > cap) return WQ_ERR_UNSUPPORTED;
+    return gemm_impl(A, packed, scales, zeros, C, M, N, K, format, group, ws, cap, stream, path);
 }
 
 WQ_EXPORT size_t wq_gemm_workspace_size(int M, int N, int K, int format, int group) {

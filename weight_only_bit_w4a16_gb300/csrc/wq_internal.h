@@ -34,6 +34,11 @@ int launch_tc(const void* A, const uint8_t* packed, const void* scales, const ui
               size_t workspace_bytes, cudaStream_t stream);
 size_t tc_workspace_bytes(int M, int N, int K);
 
+// The library's own stream-K scratch (a file-scope device array of the
+// tensor-core module) on the current device and its size; NULL if the
+// address cannot be had.
+void* static_workspace(size_t* bytes);
+
 // A kernel whose bounded wait is bound to run out (tests the failure path).
 int launch_timeout_selftest(cudaStream_t stream);
 

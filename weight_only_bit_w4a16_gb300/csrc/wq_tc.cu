@@ -671,6 +671,24 @@ TcPlan plan_tc(int M, int N, int K, int sms, bool allow_streamk) {
 
 }  // namespace
 
+// Library-owned scratch of wq_gemm_static: the stream-K flags and partials
+// of up to kStaticCtas CTAs with 128 x 256 fp32 tiles (zero at module load;
+// every completed call leaves the flags zero).
+constexpr int kStaticCtas = 160;
+constexpr size_t kStaticWsBytes = kFlagBytes(kStaticCtas) + (size_t)kStaticCtas * kBN * kBMMax * sizeof(float);
+static __device__ __align__(256) uint8_t g_static_ws[kStaticWsBytes];
+
+void* static_workspace(size_t* bytes) {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev] && cudaGetSymbolAddress(&addr[dev], g_static_ws) != cudaSuccess) addr[dev] = nullptr;
+    *bytes = addr[dev] ? kStaticWsBytes : 0;
+    return addr[dev];
+}
+
 size_t tc_workspace_bytes(int M, int N, int K) {
     if (M <= 0 || N <= 0 || K <= 0 || K % kBK != 0) return 0;
     return plan_tc(M, N, K, device_sms(), true).ws_bytes;

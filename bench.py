@@ -55,8 +55,8 @@ BENCH_WORKLOADS = {
 }
 
 KERNEL_SOURCES = {  # files whose content defines the dominant kernel of a workload
-    "decode_int4": ["wq_gemv.cu", "wq_common.cuh"],
-    "tiny_nvfp4": ["wq_gemv.cu", "wq_common.cuh"],
+    "decode_int4": ["wq_gemv_tma.cu", "wq_gemv.cuh", "wq_common.cuh"],
+    "tiny_nvfp4": ["wq_gemv_tma.cu", "wq_gemv.cuh", "wq_common.cuh"],
     "prefill_mxfp4": ["wq_tc.cu", "wq_tc.cuh", "wq_common.cuh"],
     "large_nvfp4": ["wq_tc.cu", "wq_tc.cuh", "wq_common.cuh"],
 }

@@ -121,6 +121,16 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
                  ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
+// 16 bytes global -> shared without a register round trip; src_bytes < 16
+// zero-fills the rest (0: all zeros, the source is not read)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -306,8 +316,12 @@ __device__ __forceinline__ void warp_loop(uint32_t wp, uint32_t S8, uint32_t rp,
     }
 }
 
+// One tile of activations (M <= 8) keeps to 64 registers, so that two
+// launches' CTAs fit on an SM; two tiles (M <= 16) hold 96 KB of activations
+// per CTA and never share an SM, so they take the registers to have all 16
+// rows of their activation loads in flight at once.
 template <int FMT, int NT, int MODE>
-__global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const TmaGemvArgs a) {
+__global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_stream_kernel(const TmaGemvArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 127u) & ~127u;
     uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
@@ -406,16 +420,17 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const TmaGemvArgs a
         for (int e = gt; e < nu; e += gsz) {
             const int u = u0 + e;
             const uint32_t pos = (uint32_t)a_pos(u) * 16;
-            for (int m0 = 0; m0 < Mc; m0 += 8) {
-                uint4 v[8];
+            constexpr int MB = NT * 8;   // activation rows in flight per thread
+            for (int m0 = 0; m0 < Mc; m0 += MB) {
+                uint4 v[MB];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
+                for (int q = 0; q < MB; ++q) {
                     v[q] = make_uint4(0, 0, 0, 0);
                     if (m0 + q < Mc && u < ulim)
                         v[q] = *reinterpret_cast<const uint4*>(a.A + (size_t)(mz + m0 + q) * a.K + u * 8);
                 }
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
+                for (int q = 0; q < MB; ++q) {
                     if (m0 + q < Mc) {
                         uint4 w = v[q];
                         if constexpr (MODE == kModeInt4) {
@@ -481,17 +496,19 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const TmaGemvArgs a
         }
     }
     __syncthreads();
-    for (int m = 0; m < Mc; ++m) {
-        for (int rl = tid; rl < rows; rl += blockDim.x) {
-            const int n = n0 + rl;
-            if (n >= a.N) continue;
-            const float* src = red + (size_t)m * ld + rl;
-            float v = 0.f;
-            for (int q = 0; q < Wk; ++q) v += src[(size_t)q * MP * ld];
-            const size_t o = (size_t)(mz + m) * a.N + n;
-            if (a.out_f32) static_cast<float*>(a.C)[o] = v;
-            else static_cast<__nv_bfloat16*>(a.C)[o] = __float2bfloat16_rn(v);
-        }
+    // (m, row) pairs over all threads; rows is a power of two, consecutive
+    // threads take consecutive rows (coalesced stores, conflict-free reads)
+    const int rows_log2 = 31 - __clz(rows);
+    for (int i = tid; i < Mc * rows; i += blockDim.x) {
+        const int m = i >> rows_log2, rl = i & (rows - 1);
+        const int n = n0 + rl;
+        if (n >= a.N) continue;
+        const float* src = red + (size_t)m * ld + rl;
+        float v = 0.f;
+        for (int q = 0; q < Wk; ++q) v += src[(size_t)q * MP * ld];
+        const size_t o = (size_t)(mz + m) * a.N + n;
+        if (a.out_f32) static_cast<float*>(a.C)[o] = v;
+        else static_cast<__nv_bfloat16*>(a.C)[o] = __float2bfloat16_rn(v);
     }
 }
 

@@ -345,21 +345,9 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_stream_kernel(const
     const uint32_t rec4_w = a.r4_off + (uint32_t)warp * 16 * a.R * kR4;
     const uint32_t rec_row = (uint32_t)(rr & 7) * a.R * 2 + (rr >> 3);
 
-    // ---- 1. scale / zero-point loads of the int4 g128 records -------------
-    uint32_t raw[kMaxIpw / 2];
-    if constexpr (MODE == kModeInt4) {
-        const size_t g0 = (size_t)nrow * (a.K >> 7) + it0;
-        const uint16_t* sp = static_cast<const uint16_t*>(a.scales) + g0;
-        const uint8_t* zp = a.zeros + g0;
-#pragma unroll
-        for (int t = 0; t < kMaxIpw / 2; ++t) {
-            const int j = rh + 2 * t;
-            raw[t] = 0;
-            if (j < nit) raw[t] = ldg_u16(sp + j) | (ldg_u8(zp + j) << 16);
-        }
-    }
-
-    // ---- 2. this warp's weight slice: 16 rows x its K range, one barrier --
+    // ---- 1. this warp's weight slice: 16 rows x its K range, one barrier.
+    // First thing: the release fences of the barrier set-up would otherwise
+    // wait for any loads issued before them --
     const int kb0 = it0 * 64;                                         // first packed byte of the range
     const int seg = max(0, min((it0 + nit) * 64, a.K >> 1) - kb0);    // bytes per row
     const int vrows = max(0, min(16, a.N - nb));
@@ -374,6 +362,20 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_stream_kernel(const
     if (lane < vrows && seg > 0)
         bulk_copy_g2s(sbase + a.w_off + (uint32_t)(blk * 16 + lane) * a.S + kb0,
                       a.packed + (size_t)(nb + lane) * (a.K >> 1) + kb0, (uint32_t)seg, bar);
+
+    // ---- 2. scale / zero-point loads of the int4 g128 records -------------
+    uint32_t raw[kMaxIpw / 2];
+    if constexpr (MODE == kModeInt4) {
+        const size_t g0 = (size_t)nrow * (a.K >> 7) + it0;
+        const uint16_t* sp = static_cast<const uint16_t*>(a.scales) + g0;
+        const uint8_t* zp = a.zeros + g0;
+#pragma unroll
+        for (int t = 0; t < kMaxIpw / 2; ++t) {
+            const int j = rh + 2 * t;
+            raw[t] = 0;
+            if (j < nit) raw[t] = ldg_u16(sp + j) | (ldg_u8(zp + j) << 16);
+        }
+    }
 
     // ---- 3. decode records (warp-private) ----------------------------------
     bool two = false;

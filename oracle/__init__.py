@@ -182,3 +182,75 @@ def max_threads() -> int:
 
 def set_threads(n: int) -> None:
     lib().wqo_set_threads(int(n))
+
+
+# ---------------------------------------------------------------------------
+# Fused epilogues ("fused epilogues": bias, the SiLU-gated
+# product of a gate/up projection pair, residual).  Plain fp64 definitions on
+# top of the exact product above; no arithmetic is shared with the library.
+# ---------------------------------------------------------------------------
+def silu(x):
+    """SiLU(x) = x * sigmoid(x) = x / (1 + e^-x), in fp64 (KBench spec's decoder
+    MLP: down(silu(gate(x)) * up(x)))."""
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def bf16_array(bits):
+    """bf16 bit patterns -> fp64 values, element by element through the
+    bit-by-bit decoder."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    out = np.empty(bits.shape, dtype=np.float64)
+    flat_in, flat_out = bits.reshape(-1), out.reshape(-1)
+    for i in range(flat_in.size):
+        flat_out[i] = bf16(int(flat_in[i]))
+    return out
+
+
+def gated_rows(n_weight_rows: int):
+    """Weight-row indices (gate, up) of each gated output column.  The gate
+    and up rows of one output come in interleaved groups of 8: weight rows
+    16b .. 16b+7 are the gate rows of outputs 8b .. 8b+7 and rows 16b+8 ..
+    16b+15 their up rows."""
+    assert n_weight_rows % 16 == 0
+    o = np.arange(n_weight_rows // 2)
+    gate = 16 * (o // 8) + (o % 8)
+    return gate, gate + 8
+
+
+def epilogue(C, S, bias_bits=None, residual_bits=None, gated=False, out_dtype="fp32"):
+    """Apply the fused epilogue to the exact product C (M, N weight rows) and
+    return (Y, T): the exact fp64 result and the allowed |Y_gpu - Y| per element.
+
+        y = C + bias[n]                      (bias: bf16 per weight row)
+        gated: y_o = silu(y_gate(o)) * y_up(o)  (gated_rows)
+        y += residual[m, o]                  (residual: bf16, (M, outputs))
+
+    The tolerance carries the product's gate (1e-3 S + 1e-6, fp32
+    accumulation) through the epilogue: each weight row's value may be off by
+    e = 1e-3 S + 1e-6 + 2^-22 |y|; silu has slope at most 1.0999 (its
+    derivative sigmoid(x) (1 + x (1 - sigmoid(x))) peaks there), so the gated
+    value may be off by 1.1 |u| e_g + (|silu(g)| + 1.1 e_g) e_u; the fp32
+    arithmetic of the epilogue adds 2^-19 |y|, and bf16 output 2^-8 |y|.
+    """
+    C = np.asarray(C, dtype=np.float64)
+    S = np.asarray(S, dtype=np.float64)
+    y = C.copy()
+    if bias_bits is not None:
+        y = y + bf16_array(bias_bits)[None, :]
+    e = 1e-3 * S + 1e-6 + 2.0 ** -22 * np.abs(y)
+    if gated:
+        gi, ui = gated_rows(C.shape[1])
+        g, u, eg, eu = y[:, gi], y[:, ui], e[:, gi], e[:, ui]
+        sg = silu(g)
+        y = sg * u
+        t = 1.1 * np.abs(u) * eg + (np.abs(sg) + 1.1 * eg) * eu
+    else:
+        t = e
+    if residual_bits is not None:
+        y = y + bf16_array(residual_bits)
+    t = t + 2.0 ** -19 * np.abs(y) + 1e-6
+    if out_dtype == "bf16":
+        t = t + 2.0 ** -8 * np.abs(y)
+    return y, t

@@ -28,6 +28,7 @@ oracle/) on the same workload and prints the same line with
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -394,6 +395,7 @@ def run_ours(args):
                              "roofline_frac": cb / us / 1e3 / peaks["hbm_gbs"]}
 
     e2e = run_e2e(args, w, A_by_M, weights, pool, dev, ws)
+    fused = fused_gate_up(w, dev, l2) if (w["bound"] == "hbm" and fmt == "int4" and not args.no_overlap) else None
 
     result = {
         "metric": w["metric"], "value": value, "unit": w["unit"], "n_gpus": ws,
@@ -415,10 +417,93 @@ def run_ours(args):
     }
     if per_m:
         result["per_m"] = per_m
+    if fused:
+        result["fused_gate_up"] = fused
     if rank == 0 and ws == 1:
         result["cpu_baseline"] = cpu_baseline(w, A_by_M, weights, budget_s=args.cpu_budget)
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def fused_gate_up(w, dev, l2):
+    """The decoder's gate/up projection pair (two N x K int4 weights) with the
+    SiLU-gated product, per call: one fused call (wq_gemm_fused over the
+    interleaved 2N-row weight) against two GEMV calls plus torch's silu and
+    multiply.  Graph-timed, chained launches, weights rotated past L2.  Not
+    part of the value."""
+    import torch
+    import weight_only_bit_w4a16_gb300 as wq
+    from weight_only_bit_w4a16_gb300 import metrics, synth
+    N, K, group, Ms = w["N"], w["K"], w["group"], w["Ms"]
+    gate = synth.make_weights("int4", N, K, group, seed=101)
+    up = synth.make_weights("int4", N, K, group, seed=102)
+    # interleave in groups of 8 rows: 16b..16b+7 gate rows 8b.., 16b+8.. up rows 8b..
+    order = np.empty(2 * N, dtype=np.int64)
+    o = np.arange(N)
+    order[16 * (o // 8) + (o % 8)] = o
+    order[16 * (o // 8) + 8 + (o % 8)] = N + o
+    fused_h = [np.ascontiguousarray(np.concatenate([g, u])[order]) for g, u in zip(gate, up)]
+    wb2 = 2 * metrics.weight_bytes("int4", N, K, group)
+    R = max(2, math.ceil(2.0 * l2 / wb2))
+
+    def dev_set(pk, sc, zr):
+        return (torch.from_numpy(pk).to(dev), torch.from_numpy(sc.view(np.int16)).to(dev),
+                torch.from_numpy(zr).to(dev))
+    fused_d = [dev_set(*fused_h) for _ in range(R)]
+    gate_d = [dev_set(*gate) for _ in range(R)]
+    up_d = [dev_set(*up) for _ in range(R)]
+    s = torch.cuda.Stream(dev)
+    out = {}
+    for M in Ms:
+        A = torch.randn(M, K, device=dev).to(torch.bfloat16)
+        H = torch.empty(M, N, device=dev, dtype=torch.bfloat16)
+        G = torch.empty(M, N, device=dev, dtype=torch.bfloat16)
+        U = torch.empty(M, N, device=dev, dtype=torch.bfloat16)
+        epi = wq.wq_epilogue(None, None, 1)
+        flags = wq.WQ_PATH_AUTO | wq.WQ_LAUNCH_OVERLAP
+
+        def fused_call(i, h):
+            pk, sc, zr = fused_d[i % R]
+            st = wq.wq_gemm_fused(A.data_ptr(), pk.data_ptr(), sc.data_ptr(), zr.data_ptr(), H.data_ptr(), M,
+                                  2 * N, K, wq.WQ_INT4, group, ctypes.byref(epi), None, 0, h, flags)
+            if st != wq.WQ_OK:
+                raise wq.WQError(st, "wq_gemm_fused")
+
+        def unfused_call(i, h):
+            for wset, dst in ((gate_d, G), (up_d, U)):
+                pk, sc, zr = wset[i % R]
+                st = wq.wq_gemm_ex(A.data_ptr(), pk.data_ptr(), sc.data_ptr(), zr.data_ptr(), dst.data_ptr(), M, N,
+                                   K, wq.WQ_INT4, group, h, flags)
+                if st != wq.WQ_OK:
+                    raise wq.WQError(st, "wq_gemm_ex")
+            torch.mul(torch.nn.functional.silu(G), U, out=H)
+
+        res = {}
+        for name, fn in (("fused_us", fused_call), ("unfused_us", unfused_call)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s):
+                for i in range(2):
+                    fn(i, s.cuda_stream)
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g, stream=s):
+                    for i in range(4 * R):
+                        fn(i, torch.cuda.current_stream().cuda_stream)
+            g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 20
+            with torch.cuda.stream(s):
+                e0.record(s)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(s)
+            torch.cuda.synchronize()
+            res[name] = e0.elapsed_time(e1) * 1e3 / (reps * 4 * R)
+        res["speedup"] = res["unfused_us"] / res["fused_us"]
+        res["fused_weight_GBps"] = wb2 / res["fused_us"] / 1e3
+        out[str(M)] = res
+    return {"shape": f"gate + up {N} x {K} int4 g{group} each (fused: one {2 * N}-row call, SiLU-gated "
+                     f"epilogue; unfused: two calls + torch silu and mul)", "per_m": out}
 
 
 def run_e2e(args, w, A_by_M, weights, pool, dev, ws):

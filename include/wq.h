@@ -141,6 +141,34 @@ int wq_gemm_ws(const void* A, const uint8_t* packed, const void* scales, const u
 int wq_gemm_static(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
                    void* C, int M, int N, int K, int format, int group, void* stream, int path);
 
+/*
+ * Fused epilogue (the KBench spec's decoder MLP is
+ * down(silu(gate(x)) * up(x))).  Every step is optional and runs on the
+ * fp32 accumulator of each output element before the cast to C:
+ *   y = acc + bias[n]          bias: bf16, one per weight row (N values)
+ *   gated: the SiLU-gated product of a gate/up projection pair stored as one
+ *          weight of N rows, interleaved in groups of 8: weight rows
+ *          16b .. 16b+7 are the gate rows of outputs 8b .. 8b+7 and rows
+ *          16b+8 .. 16b+15 their up rows.  Output o = silu(y_gate) * y_up,
+ *          silu(x) = x / (1 + e^-x); C then has N / 2 columns (N % 16 == 0,
+ *          else WQ_ERR_UNSUPPORTED).
+ *   y += residual[m, o]        residual: bf16, row-major, shaped like C
+ * bias and residual are device pointers, 2-byte aligned, or NULL.
+ */
+typedef struct wq_epilogue {
+    const void* bias;
+    const void* residual;
+    int gated; /* 0 or 1 */
+} wq_epilogue;
+
+/*
+ * wq_gemm_fused -- wq_gemm_ws with a fused epilogue (NULL: none).  N is the
+ * number of weight rows.  C is (M, N) or, gated, (M, N / 2).
+ */
+int wq_gemm_fused(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
+                  void* C, int M, int N, int K, int format, int group, const wq_epilogue* epilogue,
+                  void* workspace, size_t workspace_bytes, void* stream, int path);
+
 /* Workspace bytes wq_gemm_ws can use for this shape on the current device
  * (0: the shape needs none -- M <= 16, tiles that fill whole waves, or an
  * invalid description). */

@@ -105,3 +105,17 @@ def test_tensor_helpers_refuse_cpu_tensors():
     scales = torch.zeros((8, 4), dtype=torch.uint8)
     with pytest.raises(ValueError):
         wq.gemm(A, packed, scales, None, "nvfp4")
+
+
+def test_fused_argument_checks():
+    epi = wq.wq_epilogue(None, None, 1)
+    args = (FAKE, FAKE, FAKE, None, FAKE, 4, 24, 64, 0, 16)   # N = 24: not a multiple of 16
+    assert wq.wq_gemm_fused(*args, ctypes.byref(epi), None, 0, None, 0) == wq.WQ_ERR_UNSUPPORTED
+    bad = wq.wq_epilogue(None, None, 2)
+    assert wq.wq_gemm_fused(*args, ctypes.byref(bad), None, 0, None, 0) == wq.WQ_ERR_INVALID_ARG
+    odd = wq.wq_epilogue(0x10001, None, 0)
+    assert wq.wq_gemm_fused(FAKE, FAKE, FAKE, None, FAKE, 4, 32, 64, 0, 16, ctypes.byref(odd), None, 0, None,
+                            0) == wq.WQ_ERR_ALIGN
+    # M == 0 with an epilogue: validated, nothing launched
+    assert wq.wq_gemm_fused(FAKE, FAKE, FAKE, None, FAKE, 0, 32, 64, 0, 16, ctypes.byref(epi), None, 0, None,
+                            0) == wq.WQ_OK

@@ -38,12 +38,19 @@ PATHS = {"auto": WQ_PATH_AUTO, "gemv": WQ_PATH_GEMV, "tc": WQ_PATH_TC}
 
 #: the C entry points include/wq.h declares: name -> (restype, argtypes)
 _vp, _i = ctypes.c_void_p, ctypes.c_int
+class wq_epilogue(ctypes.Structure):
+    """The C struct of include/wq.h: bias, residual (device pointers or None), gated."""
+    _fields_ = [("bias", ctypes.c_void_p), ("residual", ctypes.c_void_p), ("gated", ctypes.c_int)]
+
+
 SIGNATURES = {
     "wq_gemm": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i]),
     "wq_gemm_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i]),
     "wq_gemm_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, ctypes.c_size_t, _vp, _i]),
     "wq_gemm_workspace_size": (ctypes.c_size_t, [_i, _i, _i, _i, _i]),
     "wq_gemm_static": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i]),
+    "wq_gemm_fused": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(wq_epilogue), _vp,
+                           ctypes.c_size_t, _vp, _i]),
     "wq_dequant": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "wq_get_device_error": (_i, []),
     "wq_selftest_timeout": (_i, [_vp]),
@@ -97,6 +104,12 @@ def wq_gemm_ws(A, packed, scales, zeros, C, M, N, K, format, group, workspace, w
 
 def wq_gemm_static(A, packed, scales, zeros, C, M, N, K, format, group, stream, path) -> int:
     return lib().wq_gemm_static(A, packed, scales, zeros, C, M, N, K, format, group, stream, path)
+
+
+def wq_gemm_fused(A, packed, scales, zeros, C, M, N, K, format, group, epilogue, workspace, workspace_bytes,
+                  stream, path) -> int:
+    return lib().wq_gemm_fused(A, packed, scales, zeros, C, M, N, K, format, group, epilogue, workspace,
+                               workspace_bytes, stream, path)
 
 
 def wq_gemm_workspace_size(M, N, K, format, group) -> int:
@@ -173,14 +186,15 @@ def workspace(M, N, K, fmt, group=None, device=None):
 
 
 def gemm(A, packed, scales, zeros, fmt, group=None, out_dtype="bf16", out=None, path="auto", stream=None,
-         overlap=False, workspace=None):
+         overlap=False, workspace=None, bias=None, residual=None, gated=False):
     """C = A . deq(packed, scales, zeros)^T on A's device and current stream.
 
     overlap=True sets WQ_LAUNCH_OVERLAP (programmatic dependent launch): the
     caller guarantees the preceding kernel on the stream does not write the
     weights.  workspace: a zeroed uint8 CUDA tensor (see workspace()) that
     lets the tensor-core path split tiles over the SMs; "auto" takes the
-    cached one.
+    cached one.  bias (N,) bf16, residual (M, outputs) bf16 and gated select
+    the fused epilogue of wq_gemm_fused (gated: C has N / 2 columns).
 
     A: (M, K) bf16; packed: (N, K/2) uint8; scales: (N, K/group) uint8
     (nvfp4 e4m3 / mxfp4 e8m0 bytes) or bf16 (int4); zeros: (N, K/group)
@@ -199,15 +213,28 @@ def gemm(A, packed, scales, zeros, fmt, group=None, out_dtype="bf16", out=None, 
     if A.dtype != torch.bfloat16 or packed.dtype != torch.uint8:
         raise ValueError("A must be bf16 and packed uint8")
     odt = torch.float32 if out_dtype in ("fp32", torch.float32) else torch.bfloat16
+    ncol = N // 2 if gated else N
     if out is None:
-        out = torch.empty((M, N), dtype=odt, device=A.device)
-    elif out.shape != (M, N) or out.dtype != odt:
+        out = torch.empty((M, ncol), dtype=odt, device=A.device)
+    elif out.shape != (M, ncol) or out.dtype != odt:
         raise ValueError("out has the wrong shape or dtype")
+    for t, shape in ((bias, (N,)), (residual, (M, ncol))):
+        if t is not None and (t.dtype != torch.bfloat16 or tuple(t.shape) != shape or not t.is_cuda
+                              or not t.is_contiguous()):
+            raise ValueError(f"bias / residual must be contiguous bf16 CUDA tensors of shape {shape}")
     fmt_word = f | (WQ_OUT_F32 if odt == torch.float32 else 0)
     pcode = (PATHS[path] if isinstance(path, str) else int(path)) | (WQ_LAUNCH_OVERLAP if overlap else 0)
     if isinstance(workspace, str) and workspace == "auto":
         workspace = globals()["workspace"](M, N, K, fmt, group, A.device)
-    if workspace is None:
+    if bias is not None or residual is not None or gated:
+        epi = wq_epilogue(None if bias is None else bias.data_ptr(),
+                          None if residual is None else residual.data_ptr(), 1 if gated else 0)
+        if workspace is not None and (not workspace.is_cuda or workspace.dtype != torch.uint8):
+            raise ValueError("workspace must be a uint8 CUDA tensor")
+        st = wq_gemm_fused(_ptr(A), _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(out), M, N, K, fmt_word,
+                           int(group), ctypes.byref(epi), _ptr(workspace),
+                           0 if workspace is None else workspace.numel(), _stream_handle(stream, A.device), pcode)
+    elif workspace is None:
         st = wq_gemm_ex(_ptr(A), _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(out), M, N, K, fmt_word,
                         int(group), _stream_handle(stream, A.device), pcode)
     else:

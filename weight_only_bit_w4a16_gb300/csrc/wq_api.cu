@@ -38,7 +38,7 @@ namespace {
 
 int gemm_impl(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C, int M,
               int N, int K, int format, int group, void* workspace, size_t workspace_bytes, void* stream,
-              int path) {
+              int path, const wq_epilogue* epi_in = nullptr) {
     if (format & ~(0xFF | WQ_OUT_F32)) return WQ_ERR_INVALID_ARG;
     const int fmt = format & 0xFF;
     const bool out_f32 = (format & WQ_OUT_F32) != 0;
@@ -56,16 +56,26 @@ int gemm_impl(const void* A, const uint8_t* packed, const void* scales, const ui
     if (!aligned(C, 16) || (K > 0 && !aligned(A, 16))) return WQ_ERR_ALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (workspace_bytes == 0) workspace = nullptr;
+    wq::Epilogue epi{nullptr, nullptr, 0};
+    if (epi_in) {
+        if (epi_in->gated != 0 && epi_in->gated != 1) return WQ_ERR_INVALID_ARG;
+        if (epi_in->gated && N % 16 != 0) return WQ_ERR_UNSUPPORTED;
+        if (!aligned(epi_in->bias, 2) || !aligned(epi_in->residual, 2)) return WQ_ERR_ALIGN;
+        epi.bias = static_cast<const uint16_t*>(epi_in->bias);
+        epi.residual = static_cast<const uint16_t*>(epi_in->residual);
+        epi.gated = epi_in->gated;
+    }
 
     if (path == WQ_PATH_TC)
         return wq::launch_tc(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, workspace, workspace_bytes,
-                             s);
+                             epi, s);
     if (path == WQ_PATH_AUTO && M > 16 && K > 0) {
-        st = wq::launch_tc(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, workspace, workspace_bytes, s);
+        st = wq::launch_tc(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, workspace, workspace_bytes,
+                           epi, s);
         if (st != WQ_ERR_UNSUPPORTED) return st;
         // shapes the tensor-core kernel does not take run on the GEMV kernel
     }
-    return wq::launch_gemv(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, overlap, s);
+    return wq::launch_gemv(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, overlap, epi, s);
 }
 
 }  // namespace
@@ -95,6 +105,13 @@ WQ_EXPORT int wq_gemm_static(const void* A, const uint8_t* packed, const void* s
     const size_t need = (M > 16 && N > 0 && K > 0 && K % 64 == 0) ? wq::tc_workspace_bytes(M, N, K) : 0;
     if (need > cap) return WQ_ERR_UNSUPPORTED;
     return gemm_impl(A, packed, scales, zeros, C, M, N, K, format, group, ws, cap, stream, path);
+}
+
+WQ_EXPORT int wq_gemm_fused(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C,
+                            int M, int N, int K, int format, int group, const wq_epilogue* epilogue,
+                            void* workspace, size_t workspace_bytes, void* stream, int path) {
+    return gemm_impl(A, packed, scales, zeros, C, M, N, K, format, group, workspace, workspace_bytes, stream, path,
+                     epilogue);
 }
 
 WQ_EXPORT size_t wq_gemm_workspace_size(int M, int N, int K, int format, int group) {

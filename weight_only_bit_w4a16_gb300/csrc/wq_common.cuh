@@ -262,6 +262,48 @@ __device__ __forceinline__ void int4_word_split(uint32_t w, const GroupKey& key,
     }
 }
 
+// ---------------------------------------------------------------------------
+// Fused epilogue of every GEMM kernel
+// ---------------------------------------------------------------------------
+// Optional, per output element, in fp32 before the cast to C:
+//   y = acc (+ bias[n])                              bias: bf16 per weight row
+//   gated: y = silu(y_gate) * y_up                   the SiLU-gated product of a
+//          gate/up projection pair whose rows interleave in groups of 8 --
+//          weight rows 16b .. 16b+7 are the gate rows of outputs 8b .. 8b+7,
+//          rows 16b+8 .. 16b+15 their up rows (KBench spec, the decoder MLP
+//          down(silu(gate(x)) * up(x)))
+//   y += residual[m, o]                              bf16, row-major (M, outputs)
+struct Epilogue {
+    const uint16_t* bias;
+    const uint16_t* residual;
+    int gated;
+};
+
+__device__ __forceinline__ float bf16_at(const uint16_t* p, size_t i) {
+    return __uint_as_float((uint32_t)__ldg(p + i) << 16);
+}
+
+__device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)); }
+
+// Write output (m, weight row n): v is the accumulated value of row n, u that
+// of row n + 8 (gated mode only; n must then be a gate row).  Nw: weight rows.
+__device__ __forceinline__ void store_epilogue(const Epilogue& e, void* C, int out_f32, int Nw, int m, int n,
+                                               float v, float u) {
+    float y = v;
+    if (e.bias) y += bf16_at(e.bias, n);
+    int ldc = Nw, o = n;
+    if (e.gated) {
+        if (e.bias) u += bf16_at(e.bias, n + 8);
+        y = silu_f32(y) * u;
+        ldc = Nw >> 1;
+        o = ((n >> 4) << 3) | (n & 7);
+    }
+    const size_t idx = (size_t)m * ldc + o;
+    if (e.residual) y += bf16_at(e.residual, idx);
+    if (out_f32) static_cast<float*>(C)[idx] = y;
+    else static_cast<__nv_bfloat16*>(C)[idx] = __float2bfloat16_rn(y);
+}
+
 // key of group gi from the raw scale / zero arrays
 template <int FMT>
 __device__ __forceinline__ GroupKey load_key(const void* scales, const uint8_t* zeros, size_t gi) {

@@ -56,6 +56,7 @@ struct GemvArgs {
     int its_per_cta;   // iterations per CTA of a cluster (cluster kernel) / per warp (split kernel)
     int row_blocks;    // split kernel: 16-row blocks per CTA
     int wk_log2;       // split kernel: log2 of the warps that split K for one row block
+    Epilogue epi;
 };
 
 // Scale / zero-point sources of one row: its scale bytes and zero points.
@@ -252,22 +253,22 @@ __global__ void __launch_bounds__(256) gemv_cluster_kernel(const GemvArgs a) {
         for (int rl = row0 + (int)threadIdx.x; rl < row0 + rows_mine; rl += blockDim.x) {
             const int n = n_cta + rl;
             if (n >= a.N) continue;
-            float v[MP];
+            if (a.epi.gated && (rl & 8)) continue;   // an up row: stored with its gate row
+            float v[MP], u[MP];
 #pragma unroll
-            for (int m = 0; m < MP; ++m) v[m] = 0.f;
+            for (int m = 0; m < MP; ++m) v[m] = u[m] = 0.f;
             for (int q = 0; q < ks; ++q) {
                 const float* src = cluster.map_shared_rank(red, q) + rl * MP;
 #pragma unroll
                 for (int m = 0; m < MP; ++m) v[m] += src[m];
-            }
+                if (a.epi.gated) {
 #pragma unroll
-            for (int m = 0; m < MP; ++m) {
-                if (m < Mc) {
-                    const size_t o = (size_t)(mz + m) * a.N + n;
-                    if (a.out_f32) static_cast<float*>(a.C)[o] = v[m];
-                    else static_cast<__nv_bfloat16*>(a.C)[o] = __float2bfloat16_rn(v[m]);
+                    for (int m = 0; m < MP; ++m) u[m] += src[8 * MP + m];
                 }
             }
+#pragma unroll
+            for (int m = 0; m < MP; ++m)
+                if (m < Mc) store_epilogue(a.epi, a.C, a.out_f32, a.N, mz + m, n, v[m], u[m]);
         }
         cluster.sync();   // keep this CTA's partials alive until all ranks read them
     } else {
@@ -275,12 +276,10 @@ __global__ void __launch_bounds__(256) gemv_cluster_kernel(const GemvArgs a) {
         for (int rl = threadIdx.x; rl < rows_per_cta; rl += blockDim.x) {
             const int n = n_cta + rl;
             if (n >= a.N) continue;
-            for (int m = 0; m < Mc; ++m) {
-                const float v = red[rl * MP + m];
-                const size_t o = (size_t)(mz + m) * a.N + n;
-                if (a.out_f32) static_cast<float*>(a.C)[o] = v;
-                else static_cast<__nv_bfloat16*>(a.C)[o] = __float2bfloat16_rn(v);
-            }
+            if (a.epi.gated && (rl & 8)) continue;   // an up row: stored with its gate row
+            for (int m = 0; m < Mc; ++m)
+                store_epilogue(a.epi, a.C, a.out_f32, a.N, mz + m, n, red[rl * MP + m],
+                               a.epi.gated ? red[(rl + 8) * MP + m] : 0.f);
         }
     }
 }
@@ -477,22 +476,23 @@ __global__ void __launch_bounds__(NT == 1 ? 512 : 256) gemv_kernel(const GemvArg
     for (int rl = threadIdx.x; rl < rows_per_cta; rl += blockDim.x) {
         const int n = n_cta + rl;
         if (n >= a.N) continue;
-        float v[MP];
+        if (a.epi.gated && (rl & 8)) continue;   // an up row: stored with its gate row
+        float v[MP], u[MP];
 #pragma unroll
-        for (int m = 0; m < MP; ++m) v[m] = 0.f;
+        for (int m = 0; m < MP; ++m) v[m] = u[m] = 0.f;
         for (int q = 0; q < Wk; ++q) {
             const float* src = red + ((size_t)rl * Wk + q) * MP;
 #pragma unroll
             for (int m = 0; m < MP; ++m) v[m] += src[m];
-        }
+            if (a.epi.gated) {
+                const float* up = red + ((size_t)(rl + 8) * Wk + q) * MP;
 #pragma unroll
-        for (int m = 0; m < MP; ++m) {
-            if (m < Mc) {
-                const size_t o = (size_t)(mz + m) * a.N + n;
-                if (a.out_f32) static_cast<float*>(a.C)[o] = v[m];
-                else static_cast<__nv_bfloat16*>(a.C)[o] = __float2bfloat16_rn(v[m]);
+                for (int m = 0; m < MP; ++m) u[m] += up[m];
             }
         }
+#pragma unroll
+        for (int m = 0; m < MP; ++m)
+            if (m < Mc) store_epilogue(a.epi, a.C, a.out_f32, a.N, mz + m, n, v[m], u[m]);
     }
 }
 
@@ -539,14 +539,15 @@ int launch_inst(const GemvArgs& args, dim3 grid, int threads, size_t smem, int c
 }  // namespace
 
 int launch_gemv(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C,
-                int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, cudaStream_t stream) {
+                int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, const Epilogue& epi,
+                cudaStream_t stream) {
     if (M == 0 || N == 0) return WQ_OK;
     // WQ_GEMV_KERNEL=split|cluster (tests, tuning) skips the streaming kernel
     const char* force = getenv("WQ_GEMV_KERNEL");
     const bool force_cluster = getenv("WQ_GEMV_FORCE_CLUSTER") || (force && !strcmp(force, "cluster"));
     const bool force_split = force && !strcmp(force, "split");
     if (!force_cluster && !force_split) {
-        const int st = launch_gemv_tma(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, pdl, stream);
+        const int st = launch_gemv_tma(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, pdl, epi, stream);
         if (st != WQ_ERR_UNSUPPORTED) return st;
     }
     int dev = 0, sms = 148;
@@ -573,6 +574,7 @@ int launch_gemv(const void* A, const uint8_t* packed, const void* scales, const 
     args.group = group;
     args.out_f32 = out_f32 ? 1 : 0;
     args.total_its = total_its;
+    args.epi = epi;
 
     // split-K inside one CTA when the staged activations (Mc rows, all of K)
     // leave room for two CTAs per SM

@@ -86,6 +86,7 @@ struct TmaGemvArgs {
     uint32_t S;         // shared row stride of the packed weights (bytes)
     uint32_t SA;        // shared row stride of the activations (bytes)
     uint32_t w_off, a_off, r8_off, r4_off, bar_off, red_off;
+    Epilogue epi;
 };
 
 __device__ __forceinline__ void record_gemv_timeout() { atomicExch(&g_gemv_status, WQ_ERR_DEVICE_TIMEOUT); }
@@ -498,19 +499,22 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_stream_kernel(const
         }
     }
     __syncthreads();
-    // (m, row) pairs over all threads; rows is a power of two, consecutive
-    // threads take consecutive rows (coalesced stores, conflict-free reads)
-    const int rows_log2 = 31 - __clz(rows);
-    for (int i = tid; i < Mc * rows; i += blockDim.x) {
-        const int m = i >> rows_log2, rl = i & (rows - 1);
+    // (m, output) pairs over all threads; consecutive threads take
+    // consecutive rows (coalesced stores, conflict-free reads).  Gated: an
+    // output reads its gate row 16b + j and its up row 16b + 8 + j.
+    const int outs = a.epi.gated ? rows >> 1 : rows;   // a power of two
+    const int outs_log2 = 31 - __clz(outs);
+    for (int i = tid; i < Mc * outs; i += blockDim.x) {
+        const int m = i >> outs_log2, o = i & (outs - 1);
+        const int rl = a.epi.gated ? (((o >> 3) << 4) | (o & 7)) : o;
         const int n = n0 + rl;
         if (n >= a.N) continue;
         const float* src = red + (size_t)m * ld + rl;
-        float v = 0.f;
+        float v = 0.f, u = 0.f;
         for (int q = 0; q < Wk; ++q) v += src[(size_t)q * MP * ld];
-        const size_t o = (size_t)(mz + m) * a.N + n;
-        if (a.out_f32) static_cast<float*>(a.C)[o] = v;
-        else static_cast<__nv_bfloat16*>(a.C)[o] = __float2bfloat16_rn(v);
+        if (a.epi.gated)
+            for (int q = 0; q < Wk; ++q) u += src[(size_t)q * MP * ld + 8];
+        store_epilogue(a.epi, a.C, a.out_f32, a.N, mz + m, n, v, u);
     }
 }
 
@@ -630,7 +634,8 @@ struct PlanKey {
 // this kernel: K = 0, K > 16384, or a CTA's activations + weights + records
 // above the shared-memory limit.
 int launch_gemv_tma(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C,
-                    int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, cudaStream_t stream) {
+                    int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, const Epilogue& epi,
+                    cudaStream_t stream) {
     if (M == 0 || N == 0) return WQ_OK;
     if (K <= 0 || K > kMaxIpw * (1 << kMaxWkLog2) * kItK) return WQ_ERR_UNSUPPORTED;
     const int n_its = (K + kItK - 1) / kItK;
@@ -699,6 +704,7 @@ int launch_gemv_tma(const void* A, const uint8_t* packed, const void* scales, co
     args.r4_off = plan.r4_off;
     args.bar_off = plan.bar_off;
     args.red_off = plan.red_off;
+    args.epi = epi;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((N + rows - 1) / rows, mchunks, 1);

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/wq.h"
+#include "wq_common.cuh"
 
 namespace wq {
 
@@ -16,13 +17,15 @@ int launch_dequant(const uint8_t* packed, const void* scales, const uint8_t* zer
 // pdl: launch with programmatic dependent launch (the kernel streams its
 // weights before the preceding kernel on the stream has finished)
 int launch_gemv(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
-                void* C, int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, cudaStream_t stream);
+                void* C, int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, const Epilogue& epi,
+                cudaStream_t stream);
 
 // The streaming small-M kernel (all of a CTA's weights requested by TMA up
 // front).  Returns WQ_ERR_UNSUPPORTED (without launching) for shapes it does
 // not take; launch_gemv then uses the register-streaming kernels.
 int launch_gemv_tma(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
-                    void* C, int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, cudaStream_t stream);
+                    void* C, int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, const Epilogue& epi,
+                    cudaStream_t stream);
 
 // Returns WQ_ERR_UNSUPPORTED (without launching) for shapes the tensor-core
 // kernel does not take.  With a workspace of at least tc_workspace_bytes()
@@ -31,7 +34,7 @@ int launch_gemv_tma(const void* A, const uint8_t* packed, const void* scales, co
 // CTA computes whole tiles.
 int launch_tc(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
               void* C, int M, int N, int K, int fmt, int group, bool out_f32, void* workspace,
-              size_t workspace_bytes, cudaStream_t stream);
+              size_t workspace_bytes, const Epilogue& epi, cudaStream_t stream);
 size_t tc_workspace_bytes(int M, int N, int K);
 
 // The library's own stream-K scratch (a file-scope device array of the

@@ -88,6 +88,7 @@ struct TcArgs {
     int nks;            // k-steps per tile
     long long units;    // tiles * nks
     int G;              // CTAs of a stream-K launch
+    Epilogue epi;
 };
 
 struct __align__(8) TcShared {
@@ -478,16 +479,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         f[4 * j + 3] += t.w;
                     }
                 }
-                if (n < a.N) {
-                    const int mb = m0 + ch * 32;
+                // gated: the up row of this gate row is row + 8, held by lane + 8
+                const int mb = m0 + ch * 32;
+                const bool mine = n < a.N && !(a.epi.gated && (row & 8));
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        if (mb + j < a.M) {
-                            const size_t o = (size_t)(mb + j) * a.N + n;
-                            if (a.out_f32) static_cast<float*>(a.C)[o] = f[j];
-                            else static_cast<__nv_bfloat16*>(a.C)[o] = __float2bfloat16_rn(f[j]);
-                        }
-                    }
+                for (int j = 0; j < 32; ++j) {
+                    const float u = a.epi.gated ? __shfl_xor_sync(0xffffffffu, f[j], 8) : 0.f;
+                    if (mine && mb + j < a.M) store_epilogue(a.epi, a.C, a.out_f32, a.N, mb + j, n, f[j], u);
                 }
             }
             // the accumulator may be overwritten by the next segment's MMAs
@@ -696,7 +694,7 @@ size_t tc_workspace_bytes(int M, int N, int K) {
 
 int launch_tc(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C, int M,
               int N, int K, int fmt, int group, bool out_f32, void* workspace, size_t workspace_bytes,
-              cudaStream_t stream) {
+              const Epilogue& epi, cudaStream_t stream) {
     if (M == 0 || N == 0) return WQ_OK;
     // shapes this kernel takes: whole k-steps, TMA-legal strides, aligned
     // scale rows for the per-k-step scale loads
@@ -740,6 +738,7 @@ int launch_tc(const void* A, const uint8_t* packed, const void* scales, const ui
     args.nks = plan.nks;
     args.units = plan.units;
     args.G = plan.G;
+    args.epi = epi;
     if (debug_on())
         fprintf(stderr, "wq: tcgen05 M=%d N=%d K=%d: bm=%d tiles=%d %s grid=%d\n", M, N, K, bm, plan.tiles,
                 plan.streamk ? "stream-K" : "data-parallel", plan.G);

@@ -321,7 +321,7 @@ __device__ __forceinline__ void warp_loop(uint32_t wp, uint32_t S8, uint32_t rp,
 // launches' CTAs fit on an SM; two tiles (M <= 16) hold 96 KB of activations
 // per CTA and never share an SM, so they take the registers to have all 16
 // rows of their activation loads in flight at once.
-template <int FMT, int NT, int MODE>
+template <int FMT, int NT, int MODE, bool EPI>
 __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_stream_kernel(const TmaGemvArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 127u) & ~127u;
@@ -346,9 +346,24 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_stream_kernel(const
     const uint32_t rec4_w = a.r4_off + (uint32_t)warp * 16 * a.R * kR4;
     const uint32_t rec_row = (uint32_t)(rr & 7) * a.R * 2 + (rr >> 3);
 
-    // ---- 1. this warp's weight slice: 16 rows x its K range, one barrier.
-    // First thing: the release fences of the barrier set-up would otherwise
-    // wait for any loads issued before them --
+    // ---- 1. scale / zero-point loads of the int4 g128 records -------------
+    uint32_t raw[kMaxIpw / 2];
+    if constexpr (MODE == kModeInt4) {
+        const size_t g0 = (size_t)nrow * (a.K >> 7) + it0;
+        const uint16_t* sp = static_cast<const uint16_t*>(a.scales) + g0;
+        const uint8_t* zp = a.zeros + g0;
+#pragma unroll
+        for (int t = 0; t < kMaxIpw / 2; ++t) {
+            const int j = rh + 2 * t;
+            raw[t] = 0;
+            if (j < nit) raw[t] = ldg_u16(sp + j) | (ldg_u8(zp + j) << 16);
+        }
+    }
+
+    // ---- 2. this warp's weight slice: 16 rows x its K range, one barrier
+    // (issued after the scale loads: measured faster for chained calls of one
+    // shape than the other order, whose barrier fences then wait on nothing
+    // but whose scale loads queue behind the weight stream) --
     const int kb0 = it0 * 64;                                         // first packed byte of the range
     const int seg = max(0, min((it0 + nit) * 64, a.K >> 1) - kb0);    // bytes per row
     const int vrows = max(0, min(16, a.N - nb));
@@ -363,20 +378,6 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_stream_kernel(const
     if (lane < vrows && seg > 0)
         bulk_copy_g2s(sbase + a.w_off + (uint32_t)(blk * 16 + lane) * a.S + kb0,
                       a.packed + (size_t)(nb + lane) * (a.K >> 1) + kb0, (uint32_t)seg, bar);
-
-    // ---- 2. scale / zero-point loads of the int4 g128 records -------------
-    uint32_t raw[kMaxIpw / 2];
-    if constexpr (MODE == kModeInt4) {
-        const size_t g0 = (size_t)nrow * (a.K >> 7) + it0;
-        const uint16_t* sp = static_cast<const uint16_t*>(a.scales) + g0;
-        const uint8_t* zp = a.zeros + g0;
-#pragma unroll
-        for (int t = 0; t < kMaxIpw / 2; ++t) {
-            const int j = rh + 2 * t;
-            raw[t] = 0;
-            if (j < nit) raw[t] = ldg_u16(sp + j) | (ldg_u8(zp + j) << 16);
-        }
-    }
 
     // ---- 3. decode records (warp-private) ----------------------------------
     bool two = false;
@@ -501,20 +502,29 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_stream_kernel(const
     __syncthreads();
     // (m, output) pairs over all threads; consecutive threads take
     // consecutive rows (coalesced stores, conflict-free reads).  Gated: an
-    // output reads its gate row 16b + j and its up row 16b + 8 + j.
-    const int outs = a.epi.gated ? rows >> 1 : rows;   // a power of two
+    // output reads its gate row 16b + j and its up row 16b + 8 + j.  The
+    // plain instance (EPI false) carries no epilogue code at all.
+    const bool gated = EPI && a.epi.gated;
+    const int outs = gated ? rows >> 1 : rows;   // a power of two
     const int outs_log2 = 31 - __clz(outs);
     for (int i = tid; i < Mc * outs; i += blockDim.x) {
         const int m = i >> outs_log2, o = i & (outs - 1);
-        const int rl = a.epi.gated ? (((o >> 3) << 4) | (o & 7)) : o;
+        const int rl = gated ? (((o >> 3) << 4) | (o & 7)) : o;
         const int n = n0 + rl;
         if (n >= a.N) continue;
         const float* src = red + (size_t)m * ld + rl;
-        float v = 0.f, u = 0.f;
+        float v = 0.f;
         for (int q = 0; q < Wk; ++q) v += src[(size_t)q * MP * ld];
-        if (a.epi.gated)
-            for (int q = 0; q < Wk; ++q) u += src[(size_t)q * MP * ld + 8];
-        store_epilogue(a.epi, a.C, a.out_f32, a.N, mz + m, n, v, u);
+        if constexpr (EPI) {
+            float u = 0.f;
+            if (gated)
+                for (int q = 0; q < Wk; ++q) u += src[(size_t)q * MP * ld + 8];
+            store_epilogue(a.epi, a.C, a.out_f32, a.N, mz + m, n, v, u);
+        } else {
+            const size_t o2 = (size_t)(mz + m) * a.N + n;
+            if (a.out_f32) static_cast<float*>(a.C)[o2] = v;
+            else static_cast<__nv_bfloat16*>(a.C)[o2] = __float2bfloat16_rn(v);
+        }
     }
 }
 
@@ -530,15 +540,18 @@ struct Plan {
 using KernFn = void (*)(TmaGemvArgs);
 
 template <int FMT, int NT, int MODE>
-KernFn kernel_for() {
-    return gemv_stream_kernel<FMT, NT, MODE>;
+KernFn kernel_for(bool epi) {
+    return epi ? gemv_stream_kernel<FMT, NT, MODE, true> : gemv_stream_kernel<FMT, NT, MODE, false>;
 }
 
-KernFn select_kernel(int fmt, int NT, int mode) {
-    if (fmt == kNVFP4) return NT == 1 ? kernel_for<kNVFP4, 1, kModeScaled>() : kernel_for<kNVFP4, 2, kModeScaled>();
-    if (fmt == kMXFP4) return NT == 1 ? kernel_for<kMXFP4, 1, kModeScaled>() : kernel_for<kMXFP4, 2, kModeScaled>();
-    if (mode == kModeInt4) return NT == 1 ? kernel_for<kINT4, 1, kModeInt4>() : kernel_for<kINT4, 2, kModeInt4>();
-    return NT == 1 ? kernel_for<kINT4, 1, kModeScaled>() : kernel_for<kINT4, 2, kModeScaled>();
+KernFn select_kernel(int fmt, int NT, int mode, bool epi) {
+    if (fmt == kNVFP4)
+        return NT == 1 ? kernel_for<kNVFP4, 1, kModeScaled>(epi) : kernel_for<kNVFP4, 2, kModeScaled>(epi);
+    if (fmt == kMXFP4)
+        return NT == 1 ? kernel_for<kMXFP4, 1, kModeScaled>(epi) : kernel_for<kMXFP4, 2, kModeScaled>(epi);
+    if (mode == kModeInt4)
+        return NT == 1 ? kernel_for<kINT4, 1, kModeInt4>(epi) : kernel_for<kINT4, 2, kModeInt4>(epi);
+    return NT == 1 ? kernel_for<kINT4, 1, kModeScaled>(epi) : kernel_for<kINT4, 2, kModeScaled>(epi);
 }
 
 constexpr size_t kMaxSmem = 227 * 1024;
@@ -621,10 +634,10 @@ bool choose_plan(KernFn kern, int fmt, int mode, int NT, int Mc, int mchunks, in
 }
 
 struct PlanKey {
-    int dev, fmt, mode, NT, Mc, mchunks, N, K, pdl;
+    int dev, fmt, mode, NT, Mc, mchunks, N, K, pdl, epi;
     bool operator<(const PlanKey& o) const {
-        return std::tie(dev, fmt, mode, NT, Mc, mchunks, N, K, pdl) <
-               std::tie(o.dev, o.fmt, o.mode, o.NT, o.Mc, o.mchunks, o.N, o.K, o.pdl);
+        return std::tie(dev, fmt, mode, NT, Mc, mchunks, N, K, pdl, epi) <
+               std::tie(o.dev, o.fmt, o.mode, o.NT, o.Mc, o.mchunks, o.N, o.K, o.pdl, o.epi);
     }
 };
 
@@ -648,7 +661,8 @@ int launch_gemv_tma(const void* A, const uint8_t* packed, const void* scales, co
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    KernFn kern = select_kernel(fmt, NT, mode);
+    const bool has_epi = epi.bias || epi.residual || epi.gated;
+    KernFn kern = select_kernel(fmt, NT, mode, has_epi);
 
     Plan plan;
     {
@@ -656,7 +670,7 @@ int launch_gemv_tma(const void* A, const uint8_t* packed, const void* scales, co
         static std::map<PlanKey, Plan> cache;
         static std::map<std::pair<int, KernFn>, bool> attr_set;
         const bool overridden = getenv("WQ_GEMV_RB") || getenv("WQ_GEMV_TMA_WK");
-        const PlanKey key{dev, fmt, mode, NT, Mc, mchunks, N, K, pdl ? 1 : 0};
+        const PlanKey key{dev, fmt, mode, NT, Mc, mchunks, N, K, pdl ? 1 : 0, has_epi ? 1 : 0};
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[{dev, kern}]) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem) !=

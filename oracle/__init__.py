@@ -185,8 +185,8 @@ def set_threads(n: int) -> None:
 
 
 # ---------------------------------------------------------------------------
-# Fused epilogues ("fused epilogues": bias, the SiLU-gated
-# product of a gate/up projection pair, residual).  Plain fp64 definitions on
+# Fused epilogues (bias, the SiLU-gated product of a gate/up projection pair,
+# residual; the KBench spec's decoder MLP).  Plain fp64 definitions on
 # top of the exact product above; no arithmetic is shared with the library.
 # ---------------------------------------------------------------------------
 def silu(x):

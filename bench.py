@@ -273,6 +273,11 @@ def run_ours(args):
     zeros0 = up(zeros_h)
     pool = [(packed0.clone(), scales0.clone(), None if zeros0 is None else zeros0.clone()) for _ in range(R)]
     del packed0, scales0, zeros0
+    # prepacked layout (wq_prepack, an untimed build step like the weight
+    # upload): one repacked buffer per weight set
+    prepacked = args.layout == "prepacked"
+    pre_pool = [wq.prepack(pk, sc, zr, fmt, group) for pk, sc, zr in pool] if prepacked else None
+    torch.cuda.synchronize()
     A_d = {M: up(A_by_M[M].view(np.int16)) for M in Ms}
     C_d = {M: torch.empty((M, N), dtype=odt, device=dev) for M in Ms}
     s = torch.cuda.Stream(dev)
@@ -283,10 +288,17 @@ def run_ours(args):
     overlap = wq.WQ_LAUNCH_OVERLAP if not args.no_overlap else 0
 
     def call(M, slot, stream_handle, flags=None):
+        fl = overlap if flags is None else flags
+        if prepacked:
+            st = wq.wq_gemm_prepacked(A_d[M].data_ptr(), pre_pool[slot].buf.data_ptr(), C_d[M].data_ptr(), M, N,
+                                      K, fcode, group, None, stream_handle, wq.WQ_PATH_AUTO | fl)
+            if st != wq.WQ_OK:
+                raise wq.WQError(st, "wq_gemm_prepacked")
+            return
         pk, sc, zr = pool[slot]
         st = wq.wq_gemm_ex(A_d[M].data_ptr(), pk.data_ptr(), sc.data_ptr(),
                            None if zr is None else zr.data_ptr(), C_d[M].data_ptr(), M, N, K, fcode, group,
-                           stream_handle, wq.WQ_PATH_AUTO | (overlap if flags is None else flags))
+                           stream_handle, wq.WQ_PATH_AUTO | fl)
         if st != wq.WQ_OK:
             raise wq.WQError(st, "wq_gemm_ex")
 
@@ -408,6 +420,8 @@ def run_ours(args):
                          f"({R * wb / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
                    "timing": "CUDA graphs of the timed steps, CUDA events on the launching stream",
                    "launch": "WQ_LAUNCH_OVERLAP (programmatic dependent launch)" if overlap else "plain",
+                   "layout": ("prepacked (wq_prepack, untimed build step)" if prepacked else
+                              "as given (packed, scales, zeros)"),
                    "parallelism": f"replicas x{ws}"},
         "roofline": roof, "clocks": clocks, "gpu_launches": launches, "e2e": e2e,
         "plain_launch": {"ms_per_step": plain_ms_per_step,
@@ -625,6 +639,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS), default="decode_int4")
+    ap.add_argument("--layout", choices=["prepacked", "plain"], default="plain",
+                    help="weights as given, or repacked once by wq_prepack before timing")
     ap.add_argument("--no-overlap", action="store_true",
                     help="time plain launches instead of WQ_LAUNCH_OVERLAP")
     ap.add_argument("--cpu-budget", type=float, default=15.0,

@@ -142,7 +142,7 @@ int wq_gemm_static(const void* A, const uint8_t* packed, const void* scales, con
                    void* C, int M, int N, int K, int format, int group, void* stream, int path);
 
 /*
- * Fused epilogue (SURVEY section 8f; the KBench spec's decoder MLP is
+ * Fused epilogue (the KBench spec's decoder MLP is
  * down(silu(gate(x)) * up(x))).  Every step is optional and runs on the
  * fp32 accumulator of each output element before the cast to C:
  *   y = acc + bias[n]          bias: bf16, one per weight row (N values)
@@ -173,6 +173,75 @@ int wq_gemm_fused(const void* A, const uint8_t* packed, const void* scales, cons
  * (0: the shape needs none -- M <= 16, tiles that fill whole waves, or an
  * invalid description). */
 size_t wq_gemm_workspace_size(int M, int N, int K, int format, int group);
+
+/*
+ * Offline repack ("prepack").  The KBench spec's build step may put the
+ * weights in any layout ("interleaved nibbles, pre-swizzled for your MMA
+ * fragment, scales hoisted into a separate stream"), as long as what is
+ * streamed per call is still the 4-bit codes.  wq_prepack writes such a
+ * layout once; wq_gemm_prepacked then computes the same C as wq_gemm_fused
+ * on the original arrays, reading only the prepacked buffer.
+ *
+ * Formats: WQ_NVFP4 (group 16), WQ_MXFP4 (group 32), WQ_INT4 with group 128.
+ * Other int4 groups return WQ_ERR_UNSUPPORTED.
+ *
+ * Layout (all offsets in bytes from the buffer start; Nb = ceil(N / 16) row
+ * blocks, I = ceil(K / 128) k-blocks):
+ *   codes    Nb * I blocks of 1024 bytes; block (b, i) at (b * I + i) * 1024
+ *            holds rows 16b .. 16b+15 and k = 128i .. 128i+127 as two halves
+ *            of 512 bytes, half h (k = 128i + 64h ..) at + 512h.  In a half,
+ *            row r (= weight row 16b + r) takes 32 bytes at 32r: eight 4-byte
+ *            words w0..w7, w_u holding the 8 codes k0 = 128i + 64h + 8u ..
+ *            k0 + 7, stored in the order w0 w4 w1 w5 | w2 w6 w3 w7 and with
+ *            the two 16-byte halves of the row exchanged when bit 2 of r is
+ *            set.  Inside a word: fp4 keeps the input's byte order (byte j =
+ *            k0 + 2j low nibble, k0 + 2j + 1 high nibble); int4 puts k0 + 2s
+ *            in nibble s and k0 + 2s + 1 in nibble s + 4 (s = 0..3), so one
+ *            mask of the word gives a bf16 pair of consecutive k.  Rows past
+ *            N and k past K hold code 0.
+ *   records  from Nb * I * 1024, one record block per code block, in the
+ *            same order:
+ *              WQ_INT4   96 bytes.  Bytes 0..63: row r's two uint16
+ *                        {bf16 scale, bf16 (128 + min(z, 128))} at
+ *                        8 * (r & 7) + 4 * (r >> 3); bytes 64..95: row r's
+ *                        bf16 (z - min(z, 128)) at 64 + 4 * (r & 7) +
+ *                        2 * (r >> 3) (z the zero point; both subtrahends are
+ *                        exact integers and (code - zero) is their exact
+ *                        difference from 128 + code).  Rows past N: scale 0,
+ *                        subtrahends 0x4300 (128) and 0.
+ *              WQ_NVFP4  128 bytes; row r's 8 scale bytes (groups 8i ..
+ *                        8i + 7) at 8r.  Groups past K and rows past N: 0.
+ *              WQ_MXFP4  64 bytes; row r's 4 scale bytes (groups 4i ..
+ *                        4i + 3) at 4r.  Groups past K and rows past N: 0.
+ */
+
+/* Size in bytes of the prepacked buffer for this weight, 0 for a
+ * description wq_prepack does not take (bad or unsupported format or group,
+ * K not a multiple of the group, N or K not positive). */
+size_t wq_prepack_bytes(int N, int K, int format, int group);
+
+/*
+ * wq_prepack -- write the prepacked layout of (packed, scales, zeros) into
+ * `prepacked` (device memory, 16-byte aligned, at least wq_prepack_bytes()
+ * bytes; every byte of that size is written).  Inputs as for wq_gemm.
+ * Asynchronous on `stream`.  Returns WQ_ERR_UNSUPPORTED for descriptions
+ * wq_prepack_bytes() gives 0 for, WQ_ERR_INVALID_ARG for a buffer smaller
+ * than that size, WQ_ERR_ALIGN for a misaligned buffer or input.
+ */
+int wq_prepack(const uint8_t* packed, const void* scales, const uint8_t* zeros, void* prepacked,
+               size_t prepacked_bytes, int N, int K, int format, int group, void* stream);
+
+/*
+ * wq_gemm_prepacked -- C = A . deq(B)^T for a weight B given by its
+ * prepacked buffer (N, K, format and group as passed to wq_prepack; format
+ * may carry WQ_OUT_F32).  epilogue as for wq_gemm_fused (NULL: none).
+ * `path` takes WQ_PATH_AUTO or WQ_PATH_GEMV, optionally | WQ_LAUNCH_OVERLAP;
+ * every M runs on the small-M kernel, 16 activation rows per pass.  A and C
+ * as for wq_gemm (A's rows must be 16-byte aligned: K % 8 == 0, which every
+ * supported format gives).  The buffer must be 16-byte aligned.
+ */
+int wq_gemm_prepacked(const void* A, const void* prepacked, void* C, int M, int N, int K, int format,
+                      int group, const wq_epilogue* epilogue, void* stream, int path);
 
 /*
  * wq_dequant -- W = deq(packed, scales, zeros) as an (N, K) row-major bf16

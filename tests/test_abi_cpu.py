@@ -119,3 +119,44 @@ def test_fused_argument_checks():
     # M == 0 with an epilogue: validated, nothing launched
     assert wq.wq_gemm_fused(FAKE, FAKE, FAKE, None, FAKE, 0, 32, 64, 0, 16, ctypes.byref(epi), None, 0, None,
                             0) == wq.WQ_OK
+
+
+def test_prepack_sizes_match_the_oracle_layout():
+    from oracle import prepack as opk
+    for fmt, code, group in (("int4", 2, 128), ("nvfp4", 0, 16), ("mxfp4", 1, 32)):
+        for N, K in ((20, 256), (16, 128), (8192, 3072), (1, 32 if fmt != "int4" else 128)):
+            assert wq.wq_prepack_bytes(N, K, code, group) == opk.prepack_bytes(N, K, fmt)
+    # descriptions prepack does not take
+    assert wq.wq_prepack_bytes(16, 256, 2, 64) == 0         # int4 group other than 128
+    assert wq.wq_prepack_bytes(16, 256, 0, 32) == 0         # nvfp4 group
+    assert wq.wq_prepack_bytes(0, 256, 0, 16) == 0
+    assert wq.wq_prepack_bytes(16, 0, 0, 16) == 0
+    assert wq.wq_prepack_bytes(16, 48, 0, 16) == 0          # K not a multiple of 32
+    assert wq.wq_prepack_bytes(16, 256, 0x100, 16) == 0     # flags are not a format
+
+
+def test_prepack_argument_checks():
+    nb = wq.wq_prepack_bytes(32, 256, 0, 16)
+    # (packed, scales, zeros, prepacked, bytes, N, K, format, group, stream)
+    assert wq.wq_prepack(FAKE, FAKE, None, FAKE, nb - 1, 32, 256, 0, 16, None) == wq.WQ_ERR_INVALID_ARG
+    assert wq.wq_prepack(FAKE, FAKE, None, None, nb, 32, 256, 0, 16, None) == wq.WQ_ERR_INVALID_ARG
+    assert wq.wq_prepack(FAKE, FAKE, None, ODD, nb, 32, 256, 0, 16, None) == wq.WQ_ERR_ALIGN
+    assert wq.wq_prepack(FAKE, FAKE, FAKE, FAKE, 1 << 20, 32, 256, 2, 64, None) == wq.WQ_ERR_UNSUPPORTED
+    assert wq.wq_prepack(FAKE, FAKE, FAKE, FAKE, nb, 32, 256, 0, 16, None) == wq.WQ_ERR_INVALID_ARG  # zeros for fp4
+    assert wq.wq_prepack(FAKE, FAKE, None, FAKE, nb, 32, 256, 0x100, 16, None) == wq.WQ_ERR_INVALID_ARG
+
+
+def test_gemm_prepacked_argument_checks():
+    f = wq.wq_gemm_prepacked
+    # (A, prepacked, C, M, N, K, format, group, epilogue, stream, path)
+    assert f(FAKE, FAKE, FAKE, 0, 32, 256, 0, 16, None, None, 0) == wq.WQ_OK          # M == 0: no-op
+    assert f(FAKE, FAKE, FAKE, 4, 0, 256, 0, 16, None, None, 0) == wq.WQ_OK           # N == 0: no-op
+    assert f(FAKE, FAKE, FAKE, 4, 32, 256, 0, 16, None, None, wq.WQ_PATH_TC) == wq.WQ_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, -1, 32, 256, 0, 16, None, None, 0) == wq.WQ_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, 4, 32, 256, 7, 16, None, None, 0) == wq.WQ_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, 4, 32, 256, 2, 64, None, None, 0) == wq.WQ_ERR_UNSUPPORTED
+    assert f(FAKE, ODD, FAKE, 4, 32, 256, 0, 16, None, None, 0) == wq.WQ_ERR_ALIGN
+    assert f(ODD, FAKE, FAKE, 4, 32, 256, 0, 16, None, None, 0) == wq.WQ_ERR_ALIGN
+    assert f(None, FAKE, FAKE, 4, 32, 256, 0, 16, None, None, 0) == wq.WQ_ERR_INVALID_ARG
+    epi = wq.wq_epilogue(None, None, 1)
+    assert f(FAKE, FAKE, FAKE, 4, 24, 256, 0, 16, ctypes.byref(epi), None, 0) == wq.WQ_ERR_UNSUPPORTED

@@ -1,0 +1,236 @@
+"""The prepacked weight path on the GPU: wq_prepack writes the same bytes as
+the oracle's layout writer, and wq_gemm_prepacked computes C = A . deq(B)^T
+within the method's gate against the oracle on the ORIGINAL (unpacked)
+weight -- every format, ragged N / K / M, the rare second decode steps,
+fused epilogues, chained launches and the decode configuration's full size."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import prepack as opk
+import weight_only_bit_w4a16_gb300 as wq
+from weight_only_bit_w4a16_gb300 import synth
+
+from gpu_util import assert_parity, oracle_ref, sample, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def prepack_dev(p):
+    _, packed, scales, zeros = to_dev(p)
+    pre = wq.prepack(packed, scales, zeros, p["fmt"], p["group"])
+    torch.cuda.synchronize()
+    return pre
+
+
+def run_pre(p, out="fp32", overlap=False, pre=None, **epi):
+    A, _, _, _ = to_dev(p)
+    pre = pre or prepack_dev(p)
+    C = wq.gemm_prepacked(A, pre, out_dtype=out, overlap=overlap, **epi)
+    torch.cuda.synchronize()
+    assert wq.wq_get_device_error() == wq.WQ_OK
+    return C.float().cpu().numpy().astype(np.float64)
+
+
+def check_pre(p, out="fp32", overlap=False, what=""):
+    C = run_pre(p, out, overlap)
+    Ce, S = oracle_ref(p)
+    assert_parity(C, Ce, S, out, what)
+    return C
+
+
+# -- the repack itself -----------------------------------------------------------
+@pytest.mark.parametrize("fmt,N,K", [
+    ("int4", 20, 256), ("int4", 37, 384), ("int4", 300, 3072),
+    ("nvfp4", 20, 256), ("nvfp4", 33, 160), ("nvfp4", 130, 544),
+    ("mxfp4", 20, 256), ("mxfp4", 5, 96), ("mxfp4", 100, 2080),
+])
+def test_prepack_bytes_equal_oracle(fmt, N, K):
+    p = synth.make_problem(fmt, 1, N, K, seed=N + K)
+    if fmt == "int4":   # full uint8 zero points, the second subtrahend included
+        rng = np.random.default_rng(K)
+        p["zeros"] = rng.integers(0, 256, p["zeros"].shape, dtype=np.uint8)
+    pre = prepack_dev(p)
+    want = opk.prepack(p["packed"], p["scales"], p["zeros"], fmt, p["group"])
+    got = pre.buf.cpu().numpy()
+    assert got.size == want.size
+    bad = np.flatnonzero(got != want)
+    assert bad.size == 0, f"{bad.size} bytes differ, first at {bad[:8]}"
+
+
+# -- the GEMM on prepacked weights ------------------------------------------------
+@pytest.mark.parametrize("fmt", ["int4", "nvfp4", "mxfp4"])
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16, 17, 40])
+def test_parity_against_oracle(fmt, M):
+    p = synth.make_problem(fmt, M, 256, 1024, seed=M)
+    check_pre(p, "fp32" if M % 2 else "bf16", what=f"{fmt} M={M}")
+
+
+@pytest.mark.parametrize("fmt,N,K", [("int4", 200, 384), ("int4", 8, 128), ("nvfp4", 130, 544),
+                                     ("nvfp4", 33, 160), ("mxfp4", 100, 2080), ("mxfp4", 5, 96)])
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_ragged_shapes(fmt, N, K, M):
+    """N not a multiple of 16; fp4 K not a multiple of 128 (a partial last
+    block whose activation tail the kernel zeroes)."""
+    p = synth.make_problem(fmt, M, N, K, seed=N + M)
+    check_pre(p, "fp32", what=f"{fmt} N={N} K={K} M={M}")
+
+
+@pytest.mark.parametrize("rb,wk", [("1", "0"), ("1", "3"), ("2", "1"), ("4", "2"), ("8", "1")])
+def test_cta_shapes(rb, wk, monkeypatch):
+    monkeypatch.setenv("WQ_GEMV_RB", rb)
+    monkeypatch.setenv("WQ_GEMV_TMA_WK", wk)
+    for fmt, M, N, K in (("int4", 1, 300, 3072), ("int4", 12, 200, 1024), ("nvfp4", 3, 130, 544),
+                         ("mxfp4", 16, 100, 2080)):
+        p = synth.make_problem(fmt, M, N, K, seed=int(rb) * 10 + int(wk) + M)
+        # a forced shape that cannot hold its slice is refused: at most 16
+        # blocks of 128 k per warp, at most 227 KB of shared memory
+        nk = -(-K // 128)
+        ipw = -(-nk // (1 << int(wk)))
+        warps = int(rb) << int(wk)
+        rec = 96 if fmt == "int4" else 512
+        # activation rows per CTA: 16 when they fit, else 8, 4, 2, 1
+        fits = [256 + warps * ipw * (1024 + rec) + min(M, mr) * (nk * 256 + 64) + 128 <= 227 * 1024
+                for mr in (16, 8, 4, 2, 1)]
+        if ipw > 16 or not any(fits):
+            with pytest.raises(wq.WQError) as e:
+                run_pre(p, "fp32")
+            assert e.value.status == wq.WQ_ERR_UNSUPPORTED
+            continue
+        check_pre(p, "fp32", what=f"{fmt} rb={rb} wk={wk} M={M}")
+
+
+@pytest.mark.parametrize("M", [3, 16])
+def test_int4_zero_points_above_128(M):
+    p = synth.make_problem("int4", M, 144, 1024, seed=M + 7)
+    rng = np.random.default_rng(M)
+    z = p["zeros"].copy()
+    big = rng.random(z.shape) < 0.3
+    z[big] = rng.integers(129, 256, size=int(big.sum()), dtype=np.uint8)
+    p["zeros"] = z
+    check_pre(p, "fp32", what=f"int4 big zeros M={M}")
+
+
+@pytest.mark.parametrize("M", [3, 16])
+def test_mxfp4_scales_above_2_pow_15(M):
+    p = synth.make_problem("mxfp4", M, 144, 1024, seed=M + 9)
+    rng = np.random.default_rng(M)
+    E = p["scales"].copy()
+    big = rng.random(E.shape) < 0.3
+    E[big] = rng.integers(143, 161, size=int(big.sum()), dtype=np.uint8)
+    p["scales"] = E
+    check_pre(p, "fp32", what=f"mxfp4 E>142 M={M}")
+
+
+@pytest.mark.parametrize("M", [4, 16])
+def test_int4_codes_equal_zero_give_zero(M):
+    N, K, g = 96, 512, 128
+    rng = np.random.default_rng(5)
+    z = rng.integers(0, 16, size=(N, K // g), dtype=np.uint8)
+    codes = np.repeat(z, g, axis=1)
+    p = synth.make_problem("int4", M, N, K, seed=5)
+    p.update(packed=(codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8), zeros=z)
+    assert np.all(run_pre(p, "fp32") == 0)
+
+
+@pytest.mark.parametrize("fmt", ["int4", "nvfp4"])
+def test_one_hot_activation_selects_weight(fmt):
+    """a[m, k] = 1 at one k per row: C[m, n] = w[n, k] exactly (fp32 out)."""
+    N, K = 64, 512
+    p = synth.make_problem(fmt, 16, N, K, seed=11)
+    ks = np.array([0, 1, 7, 8, 31, 64, 127, 128, 129, 200, 255, 300, 383, 384, 500, 511])
+    A = np.zeros((16, K), np.float32)
+    A[np.arange(16), ks] = 1.0
+    p["A"] = synth.bf16_bits(A)
+    W64, _ = oracle.dequant(p["packed"], p["scales"], p["zeros"], fmt, p["group"])
+    C = run_pre(p, "fp32")
+    assert np.array_equal(C, W64[:, ks].T)
+
+
+def test_deterministic_and_overlap_equal():
+    p = synth.make_problem("int4", 16, 1024, 3072, seed=9)
+    pre = prepack_dev(p)
+    C1 = run_pre(p, "fp32", pre=pre)
+    C2 = run_pre(p, "fp32", pre=pre)
+    C3 = run_pre(p, "fp32", overlap=True, pre=pre)
+    assert np.array_equal(C1, C2) and np.array_equal(C1, C3)
+
+
+def test_overlapped_launches_chain_correctly():
+    """Chained calls with WQ_LAUNCH_OVERLAP, each reading the previous call's
+    output as its activations."""
+    K = N = 1024
+    ps = [synth.make_problem("int4", 4, N, K, seed=50 + i) for i in range(3)]
+    pres = [prepack_dev(p) for p in ps]
+    x = torch.from_numpy(ps[0]["A"].view(np.int16)).view(torch.bfloat16).cuda()
+    outs = []
+    for pre in pres:
+        x = wq.gemm_prepacked(x, pre, overlap=True)
+        outs.append(x)
+    torch.cuda.synchronize()
+    a_bits = ps[0]["A"]
+    for p, o in zip(ps, outs):
+        Ce, S = oracle_ref(dict(p, A=a_bits))
+        assert_parity(o.float().cpu().numpy().astype(np.float64), Ce, S, "bf16", "prepacked overlap chain")
+        a_bits = o.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("M,K", [(16, 8192), (16, 16384), (5, 16384), (1, 16384)])
+def test_long_rows(M, K):
+    """K up to the kernel's limit; 16 activation rows of K = 8192 do not fit
+    beside the weights, so the call takes CTAs of fewer rows."""
+    p = synth.make_problem("int4", M, 96, K, seed=K + M)
+    check_pre(p, "fp32", what=f"K={K} M={M}")
+
+
+def test_k_above_limit_is_unsupported():
+    p = synth.make_problem("nvfp4", 1, 16, 16384 + 128, seed=1)
+    pre = prepack_dev(p)
+    A, _, _, _ = to_dev(p)
+    with pytest.raises(wq.WQError) as e:
+        wq.gemm_prepacked(A, pre)
+    assert e.value.status == wq.WQ_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("fmt", ["int4", "nvfp4", "mxfp4"])
+@pytest.mark.parametrize("M", [1, 16, 40])
+def test_fused_epilogue(fmt, M):
+    p = synth.make_problem(fmt, M, 256, 1024, seed=M + 3)
+    rng = np.random.default_rng(M)
+    bias = synth.bf16_bits((rng.normal(size=256) * 0.5).astype(np.float32))
+    res = synth.bf16_bits(rng.normal(size=(M, 128)).astype(np.float32))
+    dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    out = "fp32" if M % 2 else "bf16"
+    Y = run_pre(p, out, bias=dev(bias), residual=dev(res), gated=True)
+    C, S = oracle.gemm(p["A"], p["packed"], p["scales"], p["zeros"], fmt, p["group"])
+    Ye, T = oracle.epilogue(C, S, bias, res, True, out)
+    assert not (np.abs(Y - Ye) > T).any()
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_decode_workload_full_size(M):
+    """The decode configuration (int4 g128, N = 8192, K = 3072, bf16 out) in
+    the launch configuration the bench times (overlap on): oracle on sampled
+    columns (all rows)."""
+    p = synth.workload_problem("decode_int4", M=M, seed=3)
+    C = run_pre(p, "bf16", overlap=True)
+    cols = sample(p["N"], 96, M)
+    Ce, S = oracle_ref(p, cols=cols)
+    assert_parity(C[:, cols], Ce, S, "bf16", f"decode M={M}")
+
+
+def test_side_stream_and_guard_region():
+    p = synth.make_problem("nvfp4", 12, 72, 256, seed=10)
+    A, packed, scales, zeros = to_dev(p)
+    s = torch.cuda.Stream()
+    buf = torch.full((12 * 72 + 256,), 3.0, device="cuda")
+    with torch.cuda.stream(s):
+        pre = wq.prepack(packed, scales, zeros, "nvfp4")
+        wq.gemm_prepacked(A, pre, out_dtype="fp32", out=buf[: 12 * 72].view(12, 72))
+    s.synchronize()
+    assert torch.all(buf[12 * 72:] == 3.0)
+    Ce, S = oracle_ref(p)
+    assert_parity(buf[: 12 * 72].view(12, 72).cpu().numpy().astype(np.float64), Ce, S, "fp32", "side stream")

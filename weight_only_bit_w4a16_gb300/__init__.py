@@ -51,6 +51,9 @@ SIGNATURES = {
     "wq_gemm_static": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i]),
     "wq_gemm_fused": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(wq_epilogue), _vp,
                            ctypes.c_size_t, _vp, _i]),
+    "wq_prepack_bytes": (ctypes.c_size_t, [_i, _i, _i, _i]),
+    "wq_prepack": (_i, [_vp, _vp, _vp, _vp, ctypes.c_size_t, _i, _i, _i, _i, _vp]),
+    "wq_gemm_prepacked": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(wq_epilogue), _vp, _i]),
     "wq_dequant": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "wq_get_device_error": (_i, []),
     "wq_selftest_timeout": (_i, [_vp]),
@@ -114,6 +117,18 @@ def wq_gemm_fused(A, packed, scales, zeros, C, M, N, K, format, group, epilogue,
 
 def wq_gemm_workspace_size(M, N, K, format, group) -> int:
     return lib().wq_gemm_workspace_size(M, N, K, format, group)
+
+
+def wq_prepack_bytes(N, K, format, group) -> int:
+    return lib().wq_prepack_bytes(N, K, format, group)
+
+
+def wq_prepack(packed, scales, zeros, prepacked, prepacked_bytes, N, K, format, group, stream) -> int:
+    return lib().wq_prepack(packed, scales, zeros, prepacked, prepacked_bytes, N, K, format, group, stream)
+
+
+def wq_gemm_prepacked(A, prepacked, C, M, N, K, format, group, epilogue, stream, path) -> int:
+    return lib().wq_gemm_prepacked(A, prepacked, C, M, N, K, format, group, epilogue, stream, path)
 
 
 def wq_dequant(packed, scales, zeros, W, N, K, format, group, stream) -> int:
@@ -244,6 +259,71 @@ def gemm(A, packed, scales, zeros, fmt, group=None, out_dtype="bf16", out=None, 
                         int(group), _ptr(workspace), workspace.numel(), _stream_handle(stream, A.device), pcode)
     if st != WQ_OK:
         raise WQError(st, "wq_gemm")
+    return out
+
+
+class Prepacked:
+    """A weight in the prepacked layout (wq_prepack): the uint8 device buffer
+    and the description it was made from."""
+
+    def __init__(self, buf, N, K, fmt, group):
+        self.buf, self.N, self.K, self.fmt, self.group = buf, N, K, _fmt_name(fmt), group
+
+
+def prepack(packed, scales, zeros, fmt, group=None, stream=None) -> Prepacked:
+    """Repack one weight (wq_prepack) into a new uint8 CUDA tensor."""
+    import torch
+    f = _fmt(fmt)
+    group = group or DEFAULT_GROUP[_fmt_name(fmt)]
+    N, Kh = packed.shape
+    K = 2 * Kh
+    for t in (packed, scales, zeros):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    nbytes = wq_prepack_bytes(N, K, f, int(group))
+    if nbytes == 0:
+        raise WQError(WQ_ERR_UNSUPPORTED, "wq_prepack_bytes")
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=packed.device)
+    st = wq_prepack(_ptr(packed), _ptr(scales), _ptr(zeros), _ptr(buf), nbytes, N, K, f, int(group),
+                    _stream_handle(stream, packed.device))
+    if st != WQ_OK:
+        raise WQError(st, "wq_prepack")
+    return Prepacked(buf, N, K, fmt, int(group))
+
+
+def gemm_prepacked(A, pre: Prepacked, out_dtype="bf16", out=None, stream=None, overlap=False, bias=None,
+                   residual=None, gated=False):
+    """C = A . deq(B)^T for a prepacked weight (wq_gemm_prepacked); the other
+    arguments as for gemm()."""
+    import torch
+    M, K = A.shape
+    N = pre.N
+    if K != pre.K:
+        raise ValueError(f"A has K={K}, the weight K={pre.K}")
+    for t in (A, out):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    if A.dtype != torch.bfloat16:
+        raise ValueError("A must be bf16")
+    odt = torch.float32 if out_dtype in ("fp32", torch.float32) else torch.bfloat16
+    ncol = N // 2 if gated else N
+    if out is None:
+        out = torch.empty((M, ncol), dtype=odt, device=A.device)
+    elif out.shape != (M, ncol) or out.dtype != odt:
+        raise ValueError("out has the wrong shape or dtype")
+    for t, shape in ((bias, (N,)), (residual, (M, ncol))):
+        if t is not None and (t.dtype != torch.bfloat16 or tuple(t.shape) != shape or not t.is_cuda
+                              or not t.is_contiguous()):
+            raise ValueError(f"bias / residual must be contiguous bf16 CUDA tensors of shape {shape}")
+    epi = None
+    if bias is not None or residual is not None or gated:
+        epi = ctypes.byref(wq_epilogue(None if bias is None else bias.data_ptr(),
+                                       None if residual is None else residual.data_ptr(), 1 if gated else 0))
+    fmt_word = _fmt(pre.fmt) | (WQ_OUT_F32 if odt == torch.float32 else 0)
+    st = wq_gemm_prepacked(_ptr(A), _ptr(pre.buf), _ptr(out), M, N, K, fmt_word, pre.group, epi,
+                           _stream_handle(stream, A.device), WQ_LAUNCH_OVERLAP if overlap else 0)
+    if st != WQ_OK:
+        raise WQError(st, "wq_gemm_prepacked")
     return out
 
 

@@ -1,6 +1,7 @@
 // wq_api.cu -- the C ABI (include/wq.h): argument validation and kernel
 // selection.  Nothing here computes; every step of the product runs in the
-// kernels of wq_dequant.cu, wq_gemv.cu and wq_tc.cu.
+// kernels of wq_dequant.cu, wq_gemv.cu, wq_gemv_tma.cu, wq_tc.cu,
+// wq_prepack.cu and wq_gemv_pre.cu.
 #include <cstdint>
 #include <cstdlib>
 
@@ -128,6 +129,60 @@ WQ_EXPORT int wq_gemm(const void* A, const uint8_t* packed, const void* scales, 
     return wq_gemm_ex(A, packed, scales, zeros, C, M, N, K, format, group, nullptr, WQ_PATH_AUTO);
 }
 
+// prepack takes int4 g128, NVFP4 g16, MXFP4 g32 and positive N, K (K a
+// multiple of 32 and of the group, as everywhere)
+static bool prepack_desc_ok(int N, int K, int fmt, int group) {
+    if (N <= 0 || K <= 0) return false;
+    if (check_weights(reinterpret_cast<const uint8_t*>(16), reinterpret_cast<const void*>(16),
+                      fmt == WQ_INT4 ? reinterpret_cast<const uint8_t*>(16) : nullptr, N, K, fmt, group) != WQ_OK)
+        return false;
+    return fmt != WQ_INT4 || group == 128;
+}
+
+WQ_EXPORT size_t wq_prepack_bytes(int N, int K, int format, int group) {
+    if (format & ~0xFF) return 0;
+    return prepack_desc_ok(N, K, format, group) ? wq::prepack_bytes(N, K, format) : 0;
+}
+
+WQ_EXPORT int wq_prepack(const uint8_t* packed, const void* scales, const uint8_t* zeros, void* prepacked,
+                         size_t prepacked_bytes, int N, int K, int format, int group, void* stream) {
+    if (format & ~0xFF) return WQ_ERR_INVALID_ARG;
+    int st = check_weights(packed, scales, zeros, N, K, format, group);
+    if (st != WQ_OK) return st;
+    if (!prepack_desc_ok(N, K, format, group)) return WQ_ERR_UNSUPPORTED;
+    if (!prepacked) return WQ_ERR_INVALID_ARG;
+    if (prepacked_bytes < wq::prepack_bytes(N, K, format)) return WQ_ERR_INVALID_ARG;
+    if (!aligned(prepacked, 16)) return WQ_ERR_ALIGN;
+    return wq::launch_prepack(packed, scales, zeros, prepacked, N, K, format, static_cast<cudaStream_t>(stream));
+}
+
+WQ_EXPORT int wq_gemm_prepacked(const void* A, const void* prepacked, void* C, int M, int N, int K, int format,
+                                int group, const wq_epilogue* epilogue, void* stream, int path) {
+    if (format & ~(0xFF | WQ_OUT_F32)) return WQ_ERR_INVALID_ARG;
+    const int fmt = format & 0xFF;
+    if (M < 0 || N < 0 || K < 0) return WQ_ERR_INVALID_ARG;
+    if (path & ~(0xFF | WQ_LAUNCH_OVERLAP)) return WQ_ERR_INVALID_ARG;
+    const bool overlap = (path & WQ_LAUNCH_OVERLAP) != 0;
+    if ((path & 0xFF) != WQ_PATH_AUTO && (path & 0xFF) != WQ_PATH_GEMV) return WQ_ERR_INVALID_ARG;
+    if (fmt != WQ_NVFP4 && fmt != WQ_MXFP4 && fmt != WQ_INT4) return WQ_ERR_INVALID_ARG;
+    if (group <= 0) return WQ_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return WQ_OK;
+    if (!prepack_desc_ok(N, K, fmt, group)) return WQ_ERR_UNSUPPORTED;
+    if (!A || !prepacked || !C) return WQ_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(C, 16) || !aligned(prepacked, 16)) return WQ_ERR_ALIGN;
+    wq::Epilogue epi{nullptr, nullptr, 0};
+    if (epilogue) {
+        if (epilogue->gated != 0 && epilogue->gated != 1) return WQ_ERR_INVALID_ARG;
+        if (epilogue->gated && N % 16 != 0) return WQ_ERR_UNSUPPORTED;
+        if (!aligned(epilogue->bias, 2) || !aligned(epilogue->residual, 2)) return WQ_ERR_ALIGN;
+        epi.bias = static_cast<const uint16_t*>(epilogue->bias);
+        epi.residual = static_cast<const uint16_t*>(epilogue->residual);
+        epi.gated = epilogue->gated;
+    }
+    return wq::launch_gemv_prepacked(A, prepacked, C, M, N, K, fmt, (format & WQ_OUT_F32) != 0, overlap, epi,
+                                     static_cast<cudaStream_t>(stream));
+}
+
 WQ_EXPORT int wq_dequant(const uint8_t* packed, const void* scales, const uint8_t* zeros, void* W, int N, int K,
                int format, int group, void* stream) {
     if (format & ~0xFF) return WQ_ERR_INVALID_ARG;
@@ -142,7 +197,8 @@ WQ_EXPORT int wq_dequant(const uint8_t* packed, const void* scales, const uint8_
 WQ_EXPORT int wq_get_device_error(void) {
     const int a = wq::read_and_clear_device_status();
     const int b = wq::read_and_clear_gemv_status();
-    return a != 0 ? a : b;
+    const int c = wq::read_and_clear_pre_status();
+    return a != 0 ? a : (b != 0 ? b : c);
 }
 
 WQ_EXPORT int wq_selftest_timeout(void* stream) {

@@ -45,6 +45,44 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr) {
     return v;
 }
 
+__device__ __forceinline__ uint2 lds64(uint32_t saddr) {
+    uint2 v;
+    asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(saddr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds16(uint32_t saddr) {
+    uint16_t v;
+    asm("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(saddr));
+    return v;
+}
+
+// global -> shared bulk copy completing on an mbarrier (16-byte aligned
+// addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// D = A . B with a zero accumulator input (the chain starts fresh; no
+// per-iteration re-zeroing of partial sums)
+__device__ __forceinline__ void mma16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1) {
+    const float z = 0.f;
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z), "f"(z), "f"(z), "f"(z));
+}
+
 template <int FMT>
 __device__ __forceinline__ void keys_of(uint32_t raw, GroupKey& k0, GroupKey& k1) {
     if constexpr (FMT == kNVFP4) {
@@ -153,6 +191,45 @@ __device__ __forceinline__ void iteration_scaled(const uint4& qa, const uint4& q
             const uint4 bv = lds128(abase[t][j] + ioff);
             mma16816(acc[t], pa[0], pb[0], pa[1], pb[1], bv.x, bv.y);
             mma16816(acc[t], pa[2], pb[2], pa[3], pb[3], bv.z, bv.w);
+        }
+    }
+}
+
+// One iteration (16 rows x 128 k), int4 group 128: the MMAs run on the exact
+// integers (code - zero) in one chain per activation tile, the group's scale
+// multiplies the fp32 partial sums afterwards ("subtract before multiply").
+//   ap[t] : the lane's activation address for tile t in this iteration
+template <int NT, bool TWO>
+__device__ __forceinline__ void it_int4(const uint4& qa, const uint4& qb, const uint32_t (&ap)[NT],
+                                        float (&acc)[NT][4], uint32_t zzA, uint32_t zzA2, uint32_t zzB,
+                                        uint32_t zzB2, float sa, float sb) {
+    const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
+    const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
+    // CH independent MMA chains per tile (words j = h mod CH): with one tile
+    // two chains keep the dependent sequence 4 deep; two tiles already are
+    // two chains
+    constexpr int CH = NT == 1 ? 2 : 1;
+    float part[CH][NT][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t pa[4], pb[4];
+        int4_word_kk4<TWO>(wa[j], zzA, zzA2, pa);
+        int4_word_kk4<TWO>(wb[j], zzB, zzB2, pb);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const uint4 bv = lds128(ap[t] + 64 * j);
+            if (j < CH) mma16816_z(part[j % CH][t], pa[0], pb[0], pa[1], pb[1], bv.x, bv.y);
+            else mma16816(part[j % CH][t], pa[0], pb[0], pa[1], pb[1], bv.x, bv.y);
+            mma16816(part[j % CH][t], pa[2], pb[2], pa[3], pb[3], bv.z, bv.w);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float p = part[0][t][e];
+            if constexpr (CH == 2) p += part[CH - 1][t][e];
+            acc[t][e] = fmaf(e < 2 ? sa : sb, p, acc[t][e]);
         }
     }
 }

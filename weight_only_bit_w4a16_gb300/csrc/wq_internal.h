@@ -37,6 +37,15 @@ int launch_tc(const void* A, const uint8_t* packed, const void* scales, const ui
               size_t workspace_bytes, const Epilogue& epi, cudaStream_t stream);
 size_t tc_workspace_bytes(int M, int N, int K);
 
+// The prepacked layout (include/wq.h, above wq_prepack_bytes): its size,
+// the repack kernel, and the small-M kernel that reads it (any M, up to 16
+// activation rows per CTA; WQ_ERR_UNSUPPORTED for K > 16384).
+size_t prepack_bytes(int N, int K, int fmt);
+int launch_prepack(const uint8_t* packed, const void* scales, const uint8_t* zeros, void* out, int N, int K,
+                   int fmt, cudaStream_t stream);
+int launch_gemv_prepacked(const void* A, const void* prepacked, void* C, int M, int N, int K, int fmt,
+                          bool out_f32, bool pdl, const Epilogue& epi, cudaStream_t stream);
+
 // The library's own stream-K scratch (a file-scope device array of the
 // tensor-core module) on the current device and its size; NULL if the
 // address cannot be had.
@@ -49,6 +58,7 @@ int launch_timeout_selftest(cudaStream_t stream);
 // and clear; the first non-zero one wins.
 int read_and_clear_device_status();
 int read_and_clear_gemv_status();
+int read_and_clear_pre_status();
 
 // WQ_DEBUG=1 in the environment prints why a call was refused.
 bool debug_on();

@@ -55,9 +55,11 @@ BENCH_WORKLOADS = {
                        bound="hbm", metric="weight HBM GB/s (M≤16)", unit="GB/s"),
 }
 
-KERNEL_SOURCES = {  # files whose content defines the dominant kernel of a workload
+KERNEL_SOURCES = {  # files whose content defines the dominant kernel of a workload (and layout)
     "decode_int4": ["wq_gemv_tma.cu", "wq_gemv.cuh", "wq_common.cuh"],
+    "decode_int4:prepacked": ["wq_gemv_pre.cu", "wq_gemv.cuh", "wq_common.cuh"],
     "tiny_nvfp4": ["wq_gemv_tma.cu", "wq_gemv.cuh", "wq_common.cuh"],
+    "tiny_nvfp4:prepacked": ["wq_gemv_pre.cu", "wq_gemv.cuh", "wq_common.cuh"],
     "prefill_mxfp4": ["wq_tc.cu", "wq_tc.cuh", "wq_common.cuh"],
     "large_nvfp4": ["wq_tc.cu", "wq_tc.cuh", "wq_common.cuh"],
 }
@@ -276,6 +278,8 @@ def run_ours(args):
     # prepacked layout (wq_prepack, an untimed build step like the weight
     # upload): one repacked buffer per weight set
     prepacked = args.layout == "prepacked"
+    traffic_key = args.workload + (":prepacked" if prepacked and args.workload + ":prepacked" in KERNEL_SOURCES
+                                   else "")
     pre_pool = [wq.prepack(pk, sc, zr, fmt, group) for pk, sc, zr in pool] if prepacked else None
     torch.cuda.synchronize()
     A_d = {M: up(A_by_M[M].view(np.int16)) for M in Ms}
@@ -361,7 +365,7 @@ def run_ours(args):
         achieved = algo / avg_launch_s / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
+                "frac": achieved / peak, "traffic": profiled_traffic(traffic_key),
                 "algorithmic_bytes_per_launch": algo, "peak_source": peaks["source"] + " hbm_gbs"}
     else:
         flops = sum(metrics.call_flops(M, N, K) for M in Ms)
@@ -370,7 +374,7 @@ def run_ours(args):
         achieved = algo / avg_launch_s / 1e12
         peak = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
+                "frac": achieved / peak, "traffic": profiled_traffic(traffic_key),
                 "algorithmic_flops_per_launch": algo, "peak_source": peaks["source"] + " bf16_tflops (burst)"}
 
     # the same steps with plain launches (no overlap), not part of the value
@@ -406,7 +410,7 @@ def run_ours(args):
             per_m[str(M)] = {"us_per_call": us, "weight_GBps": wb / us / 1e3,
                              "roofline_frac": cb / us / 1e3 / peaks["hbm_gbs"]}
 
-    e2e = run_e2e(args, w, A_by_M, weights, pool, dev, ws)
+    e2e = run_e2e(args, w, A_by_M, weights, pool, dev, ws, pre_pool)
     fused = fused_gate_up(w, dev, l2) if (w["bound"] == "hbm" and fmt == "int4" and not args.no_overlap) else None
 
     result = {
@@ -520,12 +524,13 @@ def fused_gate_up(w, dev, l2):
                      f"epilogue; unfused: two calls + torch silu and mul)", "per_m": out}
 
 
-def run_e2e(args, w, A_by_M, weights, pool, dev, ws):
-    """The same metric through the public API (weight_only_bit_w4a16_gb300.gemm)
-    from pinned host memory.  Per step: H2D of each call's activations,
-    the calls on device-resident weights (uploaded once, as a model's weights
-    are), D2H of each result.  A second figure also uploads the weights every
-    step."""
+def run_e2e(args, w, A_by_M, weights, pool, dev, ws, pre_pool=None):
+    """The same metric through the public API (weight_only_bit_w4a16_gb300.gemm,
+    or gemm_prepacked on prepacked weights) from pinned host memory.  Per
+    step: H2D of each call's activations, the calls on device-resident
+    weights (uploaded -- and repacked -- once, as a model's weights are), D2H
+    of each result.  A second figure also uploads the weights every step
+    (and repacks them, for the prepacked layout)."""
     import torch
     import weight_only_bit_w4a16_gb300 as wq
     from weight_only_bit_w4a16_gb300 import metrics
@@ -541,14 +546,20 @@ def run_e2e(args, w, A_by_M, weights, pool, dev, ws):
 
     def one(i, upload_weights=None):
         for j, M in enumerate(Ms):
-            pk, sc, zr = pool[(i * len(Ms) + j) % R]
+            slot = (i * len(Ms) + j) % R
+            pk, sc, zr = pool[slot]
             if upload_weights is not None:
                 pk.copy_(upload_weights[0], non_blocking=True)
                 sc.copy_(upload_weights[1], non_blocking=True)
                 if zr is not None:
                     zr.copy_(upload_weights[2], non_blocking=True)
+                if pre_pool is not None:
+                    wq.prepack(pk, sc, zr, fmt, group, out=pre_pool[slot].buf)
             A_d[M].copy_(A_h[M], non_blocking=True)
-            wq.gemm(A_d[M], pk, sc, zr, fmt, group, out_dtype=out, out=C_d[M])
+            if pre_pool is not None:
+                wq.gemm_prepacked(A_d[M], pre_pool[slot], out_dtype=out, out=C_d[M])
+            else:
+                wq.gemm(A_d[M], pk, sc, zr, fmt, group, out_dtype=out, out=C_d[M])
             C_h[M].copy_(C_d[M], non_blocking=True)
 
     def timed(nsteps, upload=None):
@@ -575,7 +586,9 @@ def run_e2e(args, w, A_by_M, weights, pool, dev, ws):
     else:
         val = ws * steps * sum(metrics.call_flops(M, N, K) for M in Ms) / (ms / 1e3) / 1e12
     res = {"value": val, "unit": w["unit"], "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "steps": steps, "weights": "device-resident (uploaded once, untimed, as model weights)"}
+           "steps": steps, "weights": "device-resident (uploaded once, untimed, as model weights)" +
+                                      (", prepacked once (untimed)" if pre_pool is not None else ""),
+           "api": "gemm_prepacked" if pre_pool is not None else "gemm"}
     # every step also uploads its weights from pinned host memory
     pk_h = torch.from_numpy(weights[0]).pin_memory()
     sc_h = torch.from_numpy(weights[1].view(np.int16) if fmt == "int4" else weights[1]).pin_memory()
@@ -639,7 +652,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS), default="decode_int4")
-    ap.add_argument("--layout", choices=["prepacked", "plain"], default="plain",
+    ap.add_argument("--layout", choices=["prepacked", "plain"], default="prepacked",
                     help="weights as given, or repacked once by wq_prepack before timing")
     ap.add_argument("--no-overlap", action="store_true",
                     help="time plain launches instead of WQ_LAUNCH_OVERLAP")

@@ -270,8 +270,9 @@ class Prepacked:
         self.buf, self.N, self.K, self.fmt, self.group = buf, N, K, _fmt_name(fmt), group
 
 
-def prepack(packed, scales, zeros, fmt, group=None, stream=None) -> Prepacked:
-    """Repack one weight (wq_prepack) into a new uint8 CUDA tensor."""
+def prepack(packed, scales, zeros, fmt, group=None, stream=None, out=None) -> Prepacked:
+    """Repack one weight (wq_prepack) into a new uint8 CUDA tensor, or into
+    `out` (a uint8 CUDA tensor of at least wq_prepack_bytes() elements)."""
     import torch
     f = _fmt(fmt)
     group = group or DEFAULT_GROUP[_fmt_name(fmt)]
@@ -283,7 +284,12 @@ def prepack(packed, scales, zeros, fmt, group=None, stream=None) -> Prepacked:
     nbytes = wq_prepack_bytes(N, K, f, int(group))
     if nbytes == 0:
         raise WQError(WQ_ERR_UNSUPPORTED, "wq_prepack_bytes")
-    buf = torch.empty(nbytes, dtype=torch.uint8, device=packed.device)
+    if out is None:
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=packed.device)
+    elif out.dtype != torch.uint8 or not out.is_cuda or not out.is_contiguous() or out.numel() < nbytes:
+        raise ValueError(f"out must be a contiguous uint8 CUDA tensor of at least {nbytes} bytes")
+    else:
+        buf = out
     st = wq_prepack(_ptr(packed), _ptr(scales), _ptr(zeros), _ptr(buf), nbytes, N, K, f, int(group),
                     _stream_handle(stream, packed.device))
     if st != WQ_OK:

@@ -184,14 +184,18 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_pre_kernel(const Pr
     const int r = lane >> 2, c = lane & 3;
     const int Wk = 1 << a.wk_log2;
     const int blk = warp >> a.wk_log2, kw = warp & (Wk - 1);
-    const int rows = a.rb * 16;
-    const int n0 = blockIdx.x * rows;
-    const int b = blockIdx.x * a.rb + blk;                     // this warp's row block
+    const int rows = a.rb * 16;                                // rows of the widest CTA
+    // this CTA's row blocks: an even share of the Nb blocks (counts differ
+    // by at most one, never above rb)
+    const int bs = (int)((long long)blockIdx.x * a.Nb / gridDim.x);
+    const int be = (int)((long long)(blockIdx.x + 1) * a.Nb / gridDim.x);
+    const int n0 = bs * 16, n_end = min(a.N, be * 16);
+    const int b = bs + blk;                                    // this warp's row block
     const int mz = blockIdx.y * a.mrows;
     const int Mc = min(a.mrows, a.M - mz);
     const int it0 = kw * a.ipw;
     const int nrange = max(0, min(a.I, it0 + a.ipw) - it0);   // blocks of this K range
-    const int nit = b < a.Nb ? nrange : 0;                    // ... this warp computes
+    const int nit = b < be ? nrange : 0;                      // ... this warp computes
     const uint32_t bar = sbase + 8 * warp, abar = sbase + 128 + 8 * kw;
     const uint32_t wslice = sbase + a.w_off + (uint32_t)(warp * a.ipw) * 1024u;
     const uint32_t rslice = sbase + a.r_off + (uint32_t)(warp * a.ipw) * kRec;
@@ -343,7 +347,7 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_pre_kernel(const Pr
         const int m = i >> outs_log2, o = i & (outs - 1);
         const int rl = gated ? (((o >> 3) << 4) | (o & 7)) : o;
         const int n = n0 + rl;
-        if (n >= a.N) continue;
+        if (n >= n_end) continue;
         const float* src = red + (size_t)m * ld + rl;
         float v = 0.f;
         for (int q = 0; q < Wk; ++q) v += src[(size_t)q * MP * ld];
@@ -410,17 +414,35 @@ int env_int(const char* name, int dflt) {
     return e ? atoi(e) : dflt;
 }
 
-// The CTA shape with the streaming kernel's cost model: block iterations of
-// the busiest SM, the activation bytes it receives, one warp's run and a
-// latency round per extra wave; chained launches want room for the next
-// kernel's CTAs on every SM.
-bool choose_plan(KernFn kern, int fmt, int NT, int Mc, int mchunks, int N, int I, int sms, bool pdl, Plan& best) {
+// The CTA shape and grid.  A CTA takes an even share of the row blocks
+// (rb = the largest share) x all of K, split over Wk warps.  Cost, in SM
+// issue cycles of the busiest SM: its block iterations / 4 schedulers, the
+// activation bytes it receives, one warp's run and a latency round per extra
+// wave.  Chained launches (pdl) stream the next call's weights while this
+// one computes only if its CTAs fit beside this kernel's own; and a grid
+// smaller than the SM count lets the next call put two CTAs on an SM this
+// call left idle, which then runs twice the work -- so a grid of exactly one
+// CTA per SM is preferred there.
+bool choose_plan(KernFn kern, int fmt, int NT, int Mc, int mchunks, int Nb, int I, int sms, bool pdl, Plan& best,
+                 int& grid) {
     const int MP = NT * 8;
     const int force_rb = env_int("WQ_GEMV_RB", 0), force_wk = env_int("WQ_GEMV_TMA_WK", -1);
     const double c_it = NT == 1 ? 130.0 : 150.0;
     double best_cost = -1.0;
-    for (int rb = 1; rb <= 8; rb *= 2) {
-        if (force_rb && rb != force_rb) continue;
+    // (grid, blocks per CTA at most): fixed CTA widths, and one or two CTAs
+    // per SM with the blocks shared out evenly
+    int cg[6], crb[6], nc = 0;
+    for (int rb = 1; rb <= 8; rb *= 2, ++nc) {
+        cg[nc] = (Nb + rb - 1) / rb;
+        crb[nc] = rb;
+    }
+    for (int q = 1; q <= 2; ++q, ++nc) {
+        cg[nc] = Nb < q * sms ? Nb : q * sms;
+        crb[nc] = (Nb + cg[nc] - 1) / cg[nc];
+    }
+    for (int ci = 0; ci < nc; ++ci) {
+        const int G = cg[ci], rb = crb[ci];
+        if (rb > 8 || (force_rb && rb != force_rb)) continue;
         for (int wk = 0; wk <= kMaxWkLog2; ++wk) {
             if (force_wk >= 0 && wk != force_wk) continue;
             if ((rb << wk) * 32 > 512) continue;
@@ -430,15 +452,17 @@ bool choose_plan(KernFn kern, int fmt, int NT, int Mc, int mchunks, int N, int I
             int occ = 0;
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, p.threads, p.smem) != cudaSuccess || occ < 1)
                 continue;
-            const long long ctas = (long long)((N + rb * 16 - 1) / (rb * 16)) * mchunks;
-            const long long per_sm = (ctas + sms - 1) / sms;
+            const long long ctas = (long long)G * mchunks;
+            long long per_sm = (ctas + sms - 1) / sms;
+            if (pdl && occ >= 2 && ctas < sms) per_sm = 2;   // the next call doubles up on idle SMs
             const long long waves = (ctas + (long long)sms * occ - 1) / ((long long)sms * occ);
             double cost = per_sm * rb * I * c_it / 4.0 + per_sm * (double)Mc * I * 128 * 2 / 64.0 + p.ipw * c_it +
                           (waves - 1) * 2500.0;
-            if (pdl && occ < 2 * per_sm) cost += 4000.0;
+            if (pdl && occ < 2 * ((ctas + sms - 1) / sms)) cost += 4000.0;
             if (best_cost < 0 || cost < best_cost) {
                 best_cost = cost;
                 best = p;
+                grid = G;
             }
         }
     }
@@ -469,10 +493,10 @@ int launch_gemv_prepacked(const void* A, const void* prepacked, void* C, int M, 
     // weights, else 8, 4, 2 or 1 (one tile; long rows leave room for few)
     Plan plan;
     KernFn kern = nullptr;
-    int mrows = 0;
+    int mrows = 0, grid = 0;
     {
         static std::mutex mu;
-        static std::map<PlanKey, std::pair<Plan, bool>> cache;   // shape -> (plan, fits)
+        static std::map<PlanKey, std::tuple<Plan, int, bool>> cache;   // shape -> (plan, grid, fits)
         static std::map<std::pair<int, KernFn>, bool> attr_set;
         const bool overridden = getenv("WQ_GEMV_RB") || getenv("WQ_GEMV_TMA_WK");
         std::lock_guard<std::mutex> lock(mu);
@@ -492,11 +516,10 @@ int launch_gemv_prepacked(const void* A, const void* prepacked, void* C, int M, 
             auto it = overridden ? cache.end() : cache.find(key);
             bool fits;
             if (it != cache.end()) {
-                plan = it->second.first;
-                fits = it->second.second;
+                std::tie(plan, grid, fits) = it->second;
             } else {
-                fits = choose_plan(kf, fmt, NT, Mc, mchunks, N, I, sms, pdl, plan);
-                if (!overridden) cache[key] = {plan, fits};
+                fits = choose_plan(kf, fmt, NT, Mc, mchunks, Nb, I, sms, pdl, plan, grid);
+                if (!overridden) cache[key] = std::make_tuple(plan, grid, fits);
             }
             if (fits) {
                 kern = kf;
@@ -509,8 +532,8 @@ int launch_gemv_prepacked(const void* A, const void* prepacked, void* C, int M, 
         return WQ_ERR_UNSUPPORTED;
     }
     if (debug_on())
-        fprintf(stderr, "wq: prepacked GEMV M=%d N=%d K=%d: rows/CTA=%d rb=%d wk=%d threads=%d smem=%zu\n", M, N, K,
-                mrows, plan.rb, 1 << plan.wk_log2, plan.threads, plan.smem);
+        fprintf(stderr, "wq: prepacked GEMV M=%d N=%d K=%d: rows/CTA=%d grid=%d rb=%d wk=%d threads=%d smem=%zu\n", M,
+                N, K, mrows, grid, plan.rb, 1 << plan.wk_log2, plan.threads, plan.smem);
 
     const uint8_t* base = static_cast<const uint8_t*>(prepacked);
     PreArgs args;
@@ -536,7 +559,7 @@ int launch_gemv_prepacked(const void* A, const void* prepacked, void* C, int M, 
     args.epi = epi;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((N + plan.rb * 16 - 1) / (plan.rb * 16), (M + mrows - 1) / mrows, 1);
+    cfg.gridDim = dim3(grid, (M + mrows - 1) / mrows, 1);
     cfg.blockDim = dim3(plan.threads, 1, 1);
     cfg.dynamicSmemBytes = plan.smem;
     cfg.stream = stream;

@@ -295,7 +295,7 @@ def run_ours(args):
         fl = overlap if flags is None else flags
         if prepacked:
             st = wq.wq_gemm_prepacked(A_d[M].data_ptr(), pre_pool[slot].buf.data_ptr(), C_d[M].data_ptr(), M, N,
-                                      K, fcode, group, None, stream_handle, wq.WQ_PATH_AUTO | fl)
+                                      K, fcode, group, None, None, 0, stream_handle, wq.WQ_PATH_AUTO | fl)
             if st != wq.WQ_OK:
                 raise wq.WQError(st, "wq_gemm_prepacked")
             return

@@ -112,11 +112,13 @@ int wq_gemm_ex(const void* A, const uint8_t* packed, const void* scales, const u
  * library and computes the same sum of products as wq_gemm_ex.
  *   workspace        256-byte aligned device memory (NULL with 0 bytes: the
  *                    call behaves as wq_gemm_ex).  It must hold zeros before
- *                    its first use (cudaMemset); every completed call leaves
- *                    it zero again, so one workspace serves any number of
- *                    calls that are ordered on the device (one stream).
- *                    After a call that reported WQ_ERR_DEVICE_TIMEOUT it must
- *                    be zeroed again.
+ *                    its first use (cudaMemset).  It starts with one flag
+ *                    word per SM, which every completed call leaves zero
+ *                    again; the rest holds partial sums that a call always
+ *                    writes before it reads them.  So one workspace serves
+ *                    any number of calls that are ordered on the device (one
+ *                    stream).  After a call that reported
+ *                    WQ_ERR_DEVICE_TIMEOUT it must be zeroed again.
  *   workspace_bytes  its size; below wq_gemm_workspace_size() for this shape
  *                    the tiles run whole, as in wq_gemm_ex.
  * Returns WQ_ERR_ALIGN for a misaligned workspace, WQ_ERR_INVALID_ARG for a
@@ -234,14 +236,21 @@ int wq_prepack(const uint8_t* packed, const void* scales, const uint8_t* zeros, 
 /*
  * wq_gemm_prepacked -- C = A . deq(B)^T for a weight B given by its
  * prepacked buffer (N, K, format and group as passed to wq_prepack; format
- * may carry WQ_OUT_F32).  epilogue as for wq_gemm_fused (NULL: none).
- * `path` takes WQ_PATH_AUTO or WQ_PATH_GEMV, optionally | WQ_LAUNCH_OVERLAP;
- * every M runs on the small-M kernel, 16 activation rows per pass.  A and C
- * as for wq_gemm (A's rows must be 16-byte aligned: K % 8 == 0, which every
- * supported format gives).  The buffer must be 16-byte aligned.
+ * may carry WQ_OUT_F32).  epilogue as for wq_gemm_fused (NULL: none);
+ * workspace as for wq_gemm_ws (NULL with 0 bytes: none).  `path`:
+ *   WQ_PATH_AUTO  M <= 16: the small-M kernel; larger M: the tensor-core
+ *                 kernel (a half block of 8 row blocks is its 128-row weight
+ *                 tile), the small-M kernel where that one does not take the
+ *                 shape (K not a multiple of 64);
+ *   WQ_PATH_GEMV  the small-M kernel for every M (16 activation rows per
+ *                 pass; WQ_ERR_UNSUPPORTED for K > 16384);
+ *   WQ_PATH_TC    the tensor-core kernel;
+ * optionally | WQ_LAUNCH_OVERLAP (small-M kernel).  A and C as for wq_gemm.
+ * The buffer must be 16-byte aligned.
  */
 int wq_gemm_prepacked(const void* A, const void* prepacked, void* C, int M, int N, int K, int format,
-                      int group, const wq_epilogue* epilogue, void* stream, int path);
+                      int group, const wq_epilogue* epilogue, void* workspace, size_t workspace_bytes,
+                      void* stream, int path);
 
 /*
  * wq_dequant -- W = deq(packed, scales, zeros) as an (N, K) row-major bf16

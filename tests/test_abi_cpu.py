@@ -147,16 +147,19 @@ def test_prepack_argument_checks():
 
 
 def test_gemm_prepacked_argument_checks():
-    f = wq.wq_gemm_prepacked
-    # (A, prepacked, C, M, N, K, format, group, epilogue, stream, path)
-    assert f(FAKE, FAKE, FAKE, 0, 32, 256, 0, 16, None, None, 0) == wq.WQ_OK          # M == 0: no-op
-    assert f(FAKE, FAKE, FAKE, 4, 0, 256, 0, 16, None, None, 0) == wq.WQ_OK           # N == 0: no-op
-    assert f(FAKE, FAKE, FAKE, 4, 32, 256, 0, 16, None, None, wq.WQ_PATH_TC) == wq.WQ_ERR_INVALID_ARG
-    assert f(FAKE, FAKE, FAKE, -1, 32, 256, 0, 16, None, None, 0) == wq.WQ_ERR_INVALID_ARG
-    assert f(FAKE, FAKE, FAKE, 4, 32, 256, 7, 16, None, None, 0) == wq.WQ_ERR_INVALID_ARG
-    assert f(FAKE, FAKE, FAKE, 4, 32, 256, 2, 64, None, None, 0) == wq.WQ_ERR_UNSUPPORTED
-    assert f(FAKE, ODD, FAKE, 4, 32, 256, 0, 16, None, None, 0) == wq.WQ_ERR_ALIGN
-    assert f(ODD, FAKE, FAKE, 4, 32, 256, 0, 16, None, None, 0) == wq.WQ_ERR_ALIGN
-    assert f(None, FAKE, FAKE, 4, 32, 256, 0, 16, None, None, 0) == wq.WQ_ERR_INVALID_ARG
+    def f(A, pre, C, M, N, K, fmt, group, epi=None, ws=None, wsb=0, path=0):
+        return wq.wq_gemm_prepacked(A, pre, C, M, N, K, fmt, group, epi, ws, wsb, None, path)
+    assert f(FAKE, FAKE, FAKE, 0, 32, 256, 0, 16) == wq.WQ_OK                        # M == 0: no-op
+    assert f(FAKE, FAKE, FAKE, 4, 0, 256, 0, 16) == wq.WQ_OK                         # N == 0: no-op
+    assert f(FAKE, FAKE, FAKE, 4, 32, 256, 0, 16, path=7) == wq.WQ_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, 4, 32, 256, 0, 16, path=0x200) == wq.WQ_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, -1, 32, 256, 0, 16) == wq.WQ_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, 4, 32, 256, 7, 16) == wq.WQ_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, 4, 32, 256, 2, 64) == wq.WQ_ERR_UNSUPPORTED
+    assert f(FAKE, ODD, FAKE, 4, 32, 256, 0, 16) == wq.WQ_ERR_ALIGN
+    assert f(ODD, FAKE, FAKE, 4, 32, 256, 0, 16) == wq.WQ_ERR_ALIGN
+    assert f(None, FAKE, FAKE, 4, 32, 256, 0, 16) == wq.WQ_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, 4, 32, 256, 0, 16, ws=None, wsb=64) == wq.WQ_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, 4, 32, 256, 0, 16, ws=ODD, wsb=64) == wq.WQ_ERR_ALIGN
     epi = wq.wq_epilogue(None, None, 1)
-    assert f(FAKE, FAKE, FAKE, 4, 24, 256, 0, 16, ctypes.byref(epi), None, 0) == wq.WQ_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, 4, 24, 256, 0, 16, ctypes.byref(epi)) == wq.WQ_ERR_UNSUPPORTED

@@ -234,3 +234,113 @@ def test_side_stream_and_guard_region():
     assert torch.all(buf[12 * 72:] == 3.0)
     Ce, S = oracle_ref(p)
     assert_parity(buf[: 12 * 72].view(12, 72).cpu().numpy().astype(np.float64), Ce, S, "fp32", "side stream")
+
+
+# -- the tensor-core kernel on prepacked weights (M > 16) ---------------------------
+def run_tc(p, out="fp32", workspace=None, **epi):
+    A, _, _, _ = to_dev(p)
+    pre = prepack_dev(p)
+    C = wq.gemm_prepacked(A, pre, out_dtype=out, path="tc", workspace=workspace, **epi)
+    torch.cuda.synchronize()
+    assert wq.wq_get_device_error() == wq.WQ_OK
+    return C.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("fmt,N,K", [("int4", 256, 1024), ("int4", 200, 640), ("nvfp4", 256, 1024),
+                                     ("nvfp4", 136, 576), ("mxfp4", 256, 1024), ("mxfp4", 72, 320)])
+@pytest.mark.parametrize("M", [17, 96, 300])
+def test_tc_parity(fmt, N, K, M):
+    """Ragged N (row blocks past N read as zero by the tensor map), K with a
+    half-empty last 128-k block (fp4), several M tiles."""
+    p = synth.make_problem(fmt, M, N, K, seed=M + N)
+    C = run_tc(p, "fp32" if M % 2 else "bf16")
+    Ce, S = oracle_ref(p)
+    assert_parity(C, Ce, S, "fp32" if M % 2 else "bf16", f"tc {fmt} M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("fmt", ["int4", "nvfp4", "mxfp4"])
+def test_tc_streamk_workspace(fmt):
+    """A shape whose whole tiles fill the SMs badly runs split (stream-K) with a
+    workspace; same parity, and the workspace's flag words are left zero."""
+    M, N, K = 128, 3072, 3072
+    p = synth.make_problem(fmt, M, N, K, seed=5)
+    ws = wq.workspace(M, N, K, fmt, p["group"], torch.device("cuda:0"))
+    assert ws is not None
+    C = run_tc(p, "bf16", workspace=ws)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert int(ws[:sms * 4].count_nonzero()) == 0
+    cols = sample(N, 64, 1)
+    Ce, S = oracle_ref(p, cols=cols)
+    assert_parity(C[:, cols], Ce, S, "bf16", f"tc stream-K {fmt}")
+
+
+@pytest.mark.parametrize("M", [40, 200])
+def test_tc_second_decode_steps(M):
+    p = synth.make_problem("int4", M, 144, 1024, seed=M + 1)
+    rng = np.random.default_rng(M)
+    z = p["zeros"].copy()
+    big = rng.random(z.shape) < 0.3
+    z[big] = rng.integers(129, 256, size=int(big.sum()), dtype=np.uint8)
+    p["zeros"] = z
+    C = run_tc(p)
+    Ce, S = oracle_ref(p)
+    assert_parity(C, Ce, S, "fp32", f"tc int4 big zeros M={M}")
+    q = synth.make_problem("mxfp4", M, 144, 1024, seed=M + 2)
+    E = q["scales"].copy()
+    big = rng.random(E.shape) < 0.3
+    E[big] = rng.integers(143, 161, size=int(big.sum()), dtype=np.uint8)
+    q["scales"] = E
+    C = run_tc(q)
+    Ce, S = oracle_ref(q)
+    assert_parity(C, Ce, S, "fp32", f"tc mxfp4 E>142 M={M}")
+
+
+def test_tc_one_hot_selects_weight():
+    N, K = 128, 512
+    p = synth.make_problem("int4", 32, N, K, seed=12)
+    ks = np.arange(32) * 16 + (np.arange(32) % 16)
+    A = np.zeros((32, K), np.float32)
+    A[np.arange(32), ks] = 1.0
+    p["A"] = synth.bf16_bits(A)
+    W64, _ = oracle.dequant(p["packed"], p["scales"], p["zeros"], "int4", 128)
+    assert np.array_equal(run_tc(p), W64[:, ks].T)
+
+
+def test_tc_fused_epilogue():
+    M = 130
+    p = synth.make_problem("nvfp4", M, 256, 1024, seed=77)
+    rng = np.random.default_rng(M)
+    bias = synth.bf16_bits((rng.normal(size=256) * 0.5).astype(np.float32))
+    res = synth.bf16_bits(rng.normal(size=(M, 128)).astype(np.float32))
+    dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    Y = run_tc(p, "bf16", bias=dev(bias), residual=dev(res), gated=True)
+    C, S = oracle.gemm(p["A"], p["packed"], p["scales"], p["zeros"], "nvfp4", 16)
+    Ye, T = oracle.epilogue(C, S, bias, res, True, "bf16")
+    assert not (np.abs(Y - Ye) > T).any()
+
+
+def test_tc_prefill_workload_full_size():
+    """The prefill configuration (MXFP4, M = 2048, N = K = 3072, bf16 out) on
+    prepacked weights: oracle on sampled rows and columns."""
+    p = synth.workload_problem("prefill_mxfp4", seed=2)
+    A, _, _, _ = to_dev(p)
+    pre = prepack_dev(p)
+    C = wq.gemm_prepacked(A, pre).float().cpu().numpy().astype(np.float64)
+    assert wq.wq_get_device_error() == wq.WQ_OK
+    rows, cols = sample(p["M"], 24, 0), sample(p["N"], 24, 1)
+    Ce, S = oracle_ref(p, rows=rows)
+    assert_parity(C[rows], Ce, S, "bf16", "prefill rows")
+    Ce, S = oracle_ref(p, cols=cols)
+    assert_parity(C[:, cols], Ce, S, "bf16", "prefill cols")
+
+
+def test_auto_route_matches_both_kernels():
+    """AUTO sends M > 16 to the tensor-core kernel; the small-M kernel (forced
+    GEMV path) gives a result within the same gate."""
+    p = synth.make_problem("int4", 48, 256, 1024, seed=3)
+    A, _, _, _ = to_dev(p)
+    pre = prepack_dev(p)
+    Ce, S = oracle_ref(p)
+    for path in ("auto", "gemv", "tc"):
+        C = wq.gemm_prepacked(A, pre, out_dtype="fp32", path=path).cpu().numpy().astype(np.float64)
+        assert_parity(C, Ce, S, "fp32", f"route {path}")

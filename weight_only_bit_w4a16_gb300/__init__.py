@@ -53,7 +53,8 @@ SIGNATURES = {
                            ctypes.c_size_t, _vp, _i]),
     "wq_prepack_bytes": (ctypes.c_size_t, [_i, _i, _i, _i]),
     "wq_prepack": (_i, [_vp, _vp, _vp, _vp, ctypes.c_size_t, _i, _i, _i, _i, _vp]),
-    "wq_gemm_prepacked": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(wq_epilogue), _vp, _i]),
+    "wq_gemm_prepacked": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(wq_epilogue), _vp,
+                               ctypes.c_size_t, _vp, _i]),
     "wq_dequant": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "wq_get_device_error": (_i, []),
     "wq_selftest_timeout": (_i, [_vp]),
@@ -127,8 +128,10 @@ def wq_prepack(packed, scales, zeros, prepacked, prepacked_bytes, N, K, format, 
     return lib().wq_prepack(packed, scales, zeros, prepacked, prepacked_bytes, N, K, format, group, stream)
 
 
-def wq_gemm_prepacked(A, prepacked, C, M, N, K, format, group, epilogue, stream, path) -> int:
-    return lib().wq_gemm_prepacked(A, prepacked, C, M, N, K, format, group, epilogue, stream, path)
+def wq_gemm_prepacked(A, prepacked, C, M, N, K, format, group, epilogue, workspace, workspace_bytes, stream,
+                      path) -> int:
+    return lib().wq_gemm_prepacked(A, prepacked, C, M, N, K, format, group, epilogue, workspace, workspace_bytes,
+                                   stream, path)
 
 
 def wq_dequant(packed, scales, zeros, W, N, K, format, group, stream) -> int:
@@ -185,7 +188,7 @@ _workspaces = {}
 def workspace(M, N, K, fmt, group=None, device=None):
     """A zeroed device workspace for wq_gemm_ws on this shape (None if the
     shape needs none), cached per device and grown as needed.  Completed calls
-    leave it zero, so it is reused across calls on one stream."""
+    leave its flag words zero, so it is reused across calls on one stream."""
     import torch
     group = group or DEFAULT_GROUP[_fmt_name(fmt)]
     nbytes = wq_gemm_workspace_size(M, N, K, _fmt(fmt), int(group))
@@ -298,7 +301,7 @@ def prepack(packed, scales, zeros, fmt, group=None, stream=None, out=None) -> Pr
 
 
 def gemm_prepacked(A, pre: Prepacked, out_dtype="bf16", out=None, stream=None, overlap=False, bias=None,
-                   residual=None, gated=False):
+                   residual=None, gated=False, path="auto", workspace=None):
     """C = A . deq(B)^T for a prepacked weight (wq_gemm_prepacked); the other
     arguments as for gemm()."""
     import torch
@@ -326,8 +329,13 @@ def gemm_prepacked(A, pre: Prepacked, out_dtype="bf16", out=None, stream=None, o
         epi = ctypes.byref(wq_epilogue(None if bias is None else bias.data_ptr(),
                                        None if residual is None else residual.data_ptr(), 1 if gated else 0))
     fmt_word = _fmt(pre.fmt) | (WQ_OUT_F32 if odt == torch.float32 else 0)
-    st = wq_gemm_prepacked(_ptr(A), _ptr(pre.buf), _ptr(out), M, N, K, fmt_word, pre.group, epi,
-                           _stream_handle(stream, A.device), WQ_LAUNCH_OVERLAP if overlap else 0)
+    pcode = (PATHS[path] if isinstance(path, str) else int(path)) | (WQ_LAUNCH_OVERLAP if overlap else 0)
+    if isinstance(workspace, str) and workspace == "auto":
+        workspace = globals()["workspace"](M, N, K, pre.fmt, pre.group, A.device)
+    if workspace is not None and (not workspace.is_cuda or workspace.dtype != torch.uint8):
+        raise ValueError("workspace must be a uint8 CUDA tensor")
+    st = wq_gemm_prepacked(_ptr(A), _ptr(pre.buf), _ptr(out), M, N, K, fmt_word, pre.group, epi, _ptr(workspace),
+                           0 if workspace is None else workspace.numel(), _stream_handle(stream, A.device), pcode)
     if st != WQ_OK:
         raise WQError(st, "wq_gemm_prepacked")
     return out

@@ -157,13 +157,18 @@ WQ_EXPORT int wq_prepack(const uint8_t* packed, const void* scales, const uint8_
 }
 
 WQ_EXPORT int wq_gemm_prepacked(const void* A, const void* prepacked, void* C, int M, int N, int K, int format,
-                                int group, const wq_epilogue* epilogue, void* stream, int path) {
+                                int group, const wq_epilogue* epilogue, void* workspace, size_t workspace_bytes,
+                                void* stream, int path) {
     if (format & ~(0xFF | WQ_OUT_F32)) return WQ_ERR_INVALID_ARG;
     const int fmt = format & 0xFF;
     if (M < 0 || N < 0 || K < 0) return WQ_ERR_INVALID_ARG;
     if (path & ~(0xFF | WQ_LAUNCH_OVERLAP)) return WQ_ERR_INVALID_ARG;
     const bool overlap = (path & WQ_LAUNCH_OVERLAP) != 0;
-    if ((path & 0xFF) != WQ_PATH_AUTO && (path & 0xFF) != WQ_PATH_GEMV) return WQ_ERR_INVALID_ARG;
+    const int route = path & 0xFF;
+    if (route != WQ_PATH_AUTO && route != WQ_PATH_GEMV && route != WQ_PATH_TC) return WQ_ERR_INVALID_ARG;
+    if (workspace_bytes > 0 && !workspace) return WQ_ERR_INVALID_ARG;
+    if (workspace && !aligned(workspace, 256)) return WQ_ERR_ALIGN;
+    if (workspace_bytes == 0) workspace = nullptr;
     if (fmt != WQ_NVFP4 && fmt != WQ_MXFP4 && fmt != WQ_INT4) return WQ_ERR_INVALID_ARG;
     if (group <= 0) return WQ_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return WQ_OK;
@@ -179,8 +184,17 @@ WQ_EXPORT int wq_gemm_prepacked(const void* A, const void* prepacked, void* C, i
         epi.residual = static_cast<const uint16_t*>(epilogue->residual);
         epi.gated = epilogue->gated;
     }
-    return wq::launch_gemv_prepacked(A, prepacked, C, M, N, K, fmt, (format & WQ_OUT_F32) != 0, overlap, epi,
-                                     static_cast<cudaStream_t>(stream));
+    const bool out_f32 = (format & WQ_OUT_F32) != 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (route == WQ_PATH_TC)
+        return wq::launch_tc_prepacked(A, prepacked, C, M, N, K, fmt, group, out_f32, workspace, workspace_bytes,
+                                       epi, s);
+    if (route == WQ_PATH_AUTO && M > 16) {
+        const int st = wq::launch_tc_prepacked(A, prepacked, C, M, N, K, fmt, group, out_f32, workspace,
+                                               workspace_bytes, epi, s);
+        if (st != WQ_ERR_UNSUPPORTED) return st;
+    }
+    return wq::launch_gemv_prepacked(A, prepacked, C, M, N, K, fmt, out_f32, overlap, epi, s);
 }
 
 WQ_EXPORT int wq_dequant(const uint8_t* packed, const void* scales, const uint8_t* zeros, void* W, int N, int K,

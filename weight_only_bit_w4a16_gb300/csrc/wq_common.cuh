@@ -92,6 +92,12 @@ __device__ __forceinline__ uint32_t ldg_u8(const uint8_t* p) {
     return v;
 }
 
+__device__ __forceinline__ uint32_t ldg_u32(const void* p) {
+    uint32_t v;
+    asm("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t ldg_u16(const void* p) {
     uint16_t v;
     asm("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
@@ -215,6 +221,33 @@ __device__ __forceinline__ void int4_word_centered(uint32_t w, const GroupKey& k
     }
 }
 
+// int4 codes of one word minus the zero point, as exact bf16 integers, with
+// nibble s paired with nibble s + 4: (n0,n4), (n1,n5), (n2,n6), (n3,n7).  In
+// the input layout these are the k pairs (k, k+4); the prepacked layout
+// stores k0 + 2s in nibble s and k0 + 2s + 1 in nibble s + 4, so there they
+// are natural pairs.  The exponent-bias trick makes bf16(128 + code) with one
+// mask-and-or, and one exact bf16x2 subtraction of (128 + zero) leaves
+// (code - zero).  Zero points above 128 take a second exact subtraction (TWO).
+// (x & 0x000F000F) | magic as one lop3 with the magic in a register
+__device__ __forceinline__ uint32_t nib_or_magic(uint32_t x, uint32_t magic) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(d) : "r"(x), "r"(magic));
+    return d;
+}
+
+template <bool TWO>
+__device__ __forceinline__ void int4_word_kk4(uint32_t w, uint32_t zz, uint32_t zz2, uint32_t (&p)[4]) {
+    const uint32_t magic = 0x43004300u;
+    p[0] = bf16x2_sub(nib_or_magic(w, magic), zz);
+    p[1] = bf16x2_sub(nib_or_magic(w >> 4, magic), zz);
+    p[2] = bf16x2_sub(nib_or_magic(w >> 8, magic), zz);
+    p[3] = bf16x2_sub(nib_or_magic(w >> 12, magic), zz);
+    if constexpr (TWO) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) p[i] = bf16x2_sub(p[i], zz2);
+    }
+}
+
 // e2m1 codes as bf16 values times 2^-112 (exact), natural pairs
 __device__ __forceinline__ void e2m1_word_raw(uint32_t w, uint32_t (&p)[4]) {
     uint32_t h[4];
@@ -255,6 +288,20 @@ template <bool TWO>
 __device__ __forceinline__ void int4_word_split(uint32_t w, const GroupKey& key, uint32_t (&hi)[4], uint32_t (&lo)[4]) {
     uint32_t x[4];
     int4_word_centered<TWO>(w, key, x);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        hi[i] = bf16x2_mul(x[i], key.mul);
+        lo[i] = bf16x2_fma(x[i], key.mul, hi[i] ^ 0x80008000u);
+    }
+}
+
+// The same split for a prepacked int4 word (k0 + 2s in nibble s, k0 + 2s + 1
+// in nibble s + 4): natural pairs straight from the nibble pairs.
+template <bool TWO>
+__device__ __forceinline__ void int4_word_split_pairs(uint32_t w, const GroupKey& key, uint32_t (&hi)[4],
+                                                      uint32_t (&lo)[4]) {
+    uint32_t x[4];
+    int4_word_kk4<TWO>(w, key.zz, key.zz2, x);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         hi[i] = bf16x2_mul(x[i], key.mul);

@@ -97,31 +97,6 @@ __device__ __forceinline__ void keys_of(uint32_t raw, GroupKey& k0, GroupKey& k1
     }
 }
 
-// int4 codes of one word minus the zero point, as exact bf16 integers, in
-// the (k, k+4) pair order: (k0,k4), (k1,k5), (k2,k6), (k3,k7).  The
-// exponent-bias trick makes bf16(128 + code) with one mask-and-or, and one
-// exact bf16x2 subtraction of (128 + zero) leaves (code - zero).  Zero points
-// above 128 take a second exact subtraction (TWO).
-// (x & 0x000F000F) | magic as one lop3 with the magic in a register
-__device__ __forceinline__ uint32_t nib_or_magic(uint32_t x, uint32_t magic) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(d) : "r"(x), "r"(magic));
-    return d;
-}
-
-template <bool TWO>
-__device__ __forceinline__ void int4_word_kk4(uint32_t w, uint32_t zz, uint32_t zz2, uint32_t (&p)[4]) {
-    const uint32_t magic = 0x43004300u;
-    p[0] = bf16x2_sub(nib_or_magic(w, magic), zz);
-    p[1] = bf16x2_sub(nib_or_magic(w >> 4, magic), zz);
-    p[2] = bf16x2_sub(nib_or_magic(w >> 8, magic), zz);
-    p[3] = bf16x2_sub(nib_or_magic(w >> 12, magic), zz);
-    if constexpr (TWO) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) p[i] = bf16x2_sub(p[i], zz2);
-    }
-}
-
 // bf16x2 subtrahends of a zero point: (128 + z) for z <= 128 (0x4300 + z is
 // exactly 128 + z, the carry of z = 128 moving into the exponent), else 128
 // and then z itself

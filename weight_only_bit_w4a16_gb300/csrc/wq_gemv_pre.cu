@@ -84,12 +84,6 @@ __device__ __forceinline__ void sts128_zero(uint32_t saddr) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(saddr), "r"(0) : "memory");
 }
 
-__device__ __forceinline__ uint32_t ldg_u32(const uint8_t* p) {
-    uint32_t v;
-    asm("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
-
 // The lane's four words of one 128-k block, rows r (qa) and r + 8 (qb), in
 // the order of the k units c, c + 4, c + 8, c + 12.  wp: the lane's 8 bytes
 // of half 0, row r (row r + 8 is 256 bytes on, half 1 is 512 bytes on).

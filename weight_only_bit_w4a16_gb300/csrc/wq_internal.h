@@ -37,6 +37,12 @@ int launch_tc(const void* A, const uint8_t* packed, const void* scales, const ui
               size_t workspace_bytes, const Epilogue& epi, cudaStream_t stream);
 size_t tc_workspace_bytes(int M, int N, int K);
 
+// The tensor-core kernel on prepacked weights (same contract as launch_tc;
+// one k-step of 128 rows is 8 row blocks' half blocks).
+int launch_tc_prepacked(const void* A, const void* prepacked, void* C, int M, int N, int K, int fmt, int group,
+                        bool out_f32, void* workspace, size_t workspace_bytes, const Epilogue& epi,
+                        cudaStream_t stream);
+
 // The prepacked layout (include/wq.h, above wq_prepack_bytes): its size,
 // the repack kernel, and the small-M kernel that reads it (any M, up to 16
 // activation rows per CTA; WQ_ERR_UNSUPPORTED for K > 16384).

@@ -73,7 +73,7 @@ constexpr uint64_t kDrainNs = 100000000ull;        // 0.1 s
 static_assert(kAccCols + kWBufs * kWCols <= kTmemCols, "TMEM budget");
 
 struct TcArgs {
-    const uint8_t* scales;
+    const uint8_t* scales;   // prepacked weights: the record blocks
     const uint8_t* zeros;
     void* C;
     float* ws;          // stream-K partial sums [G][bm / 32][8][128] float4; null: one tile per CTA
@@ -88,6 +88,7 @@ struct TcArgs {
     int nks;            // k-steps per tile
     long long units;    // tiles * nks
     int G;              // CTAs of a stream-K launch
+    int kblocks;        // prepacked weights: 128-k blocks per row
     Epilogue epi;
 };
 
@@ -187,6 +188,69 @@ __device__ __forceinline__ void decode_row(const uint4& c0, const uint4& c1, con
     }
 }
 
+// The same raw scale data from a prepacked weight's record blocks (block
+// (n / 16, ks / 2), row n % 16, half ks % 2):
+//   nvfp4: the 4 bytes of groups 4ks..4ks+3 (the row's 8 bytes at 8 r)
+//   mxfp4: the 2 bytes of groups 2ks, 2ks+1 (the row's 4 bytes at 4 r)
+//   int4 : {bf16 scale | bf16 (128 + min(z, 128)) << 16}, bf16 (z - min(z, 128))
+template <int FMT>
+__device__ __forceinline__ uint2 tc_raw_pre(const TcArgs& a, int n, int ks) {
+    const size_t blk = (size_t)(n >> 4) * a.kblocks + (ks >> 1);
+    const int r = n & 15, h = ks & 1;
+    uint2 raw;
+    if constexpr (FMT == kNVFP4) {
+        raw.x = ldg_u32(a.scales + blk * 128 + 8 * r + 4 * h);
+        raw.y = 0;
+    } else if constexpr (FMT == kMXFP4) {
+        raw.x = ldg_u16(a.scales + blk * 64 + 4 * r + 2 * h);
+        raw.y = 0;
+    } else {
+        const uint8_t* rec = a.scales + blk * 96;
+        raw.x = ldg_u32(rec + 8 * (r & 7) + 4 * (r >> 3));
+        raw.y = ldg_u16(rec + 64 + 4 * (r & 7) + 2 * (r >> 3));
+    }
+    return raw;
+}
+
+template <int FMT>
+__device__ __forceinline__ void tc_keys_pre(uint2 raw, GroupKey (&key)[4]) {
+    if constexpr (FMT == kINT4) {
+        GroupKey k;
+        k.mul = splat16(raw.x);
+        k.mul2 = 0x3F803F80u;
+        k.zz = splat16(raw.x >> 16);
+        k.zz2 = splat16(raw.y);
+        k.two = (raw.y & 0xFFFFu) != 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) key[j] = k;
+    } else {
+        tc_keys<FMT>(raw, key);   // the same bytes as the input layout's
+    }
+}
+
+// One row's 64 weights of a k-step from the prepacked layout: the row's two
+// 16-byte chunks hold the words w0 w4 w1 w5 | w2 w6 w3 w7; int4 words hold
+// natural k pairs in nibbles (s, s + 4).
+template <int FMT, bool TWO>
+__device__ __forceinline__ void decode_row_pre(const uint4& c0, const uint4& c1, const GroupKey (&key)[4],
+                                               uint32_t (&w)[32], uint32_t (&w2)[32]) {
+    const uint32_t wd[8] = {c0.x, c0.z, c1.x, c1.z, c0.y, c0.w, c1.y, c1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t p[4], r[4];
+        if constexpr (FMT == kINT4) {
+            int4_word_split_pairs<TWO>(wd[i], key_of_word<FMT>(key, i), p, r);
+        } else {
+            word_scaled<FMT, TWO>(wd[i], key_of_word<FMT>(key, i), p);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            w[4 * i + e] = p[e];
+            if constexpr (FMT == kINT4) w2[4 * i + e] = r[e];
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // work split
 // ---------------------------------------------------------------------------
@@ -258,7 +322,10 @@ __device__ __forceinline__ bool wait_flag(const unsigned* f, volatile int* abort
     }
 }
 
-template <int FMT>
+// PRE: the weights are in the prepacked layout (tmapP a 3-D map of its code
+// blocks: 512-byte half blocks x 2 per 128-k block x row blocks; scales
+// from its record blocks)
+template <int FMT, bool PRE>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap tmapA, const __grid_constant__ CUtensorMap tmapP, const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -318,7 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb = smem_u32(&sh.full[s]);
                     mbar_arrive_expect_tx(fb, kStageBytes);
                     tma_load_2d(smem_u32(st), &tmapA, fb, k * kBK, m0);
-                    tma_load_2d(smem_u32(st + kATileBytes), &tmapP, fb, k * (kBK / 2), n0);
+                    if constexpr (PRE) tma_load_3d(smem_u32(st + kATileBytes), &tmapP, fb, 0, k, n0 >> 4);
+                    else tma_load_2d(smem_u32(st + kATileBytes), &tmapP, fb, k * (kBK / 2), n0);
                 }
             }
             // never leave the CTA with copies in flight
@@ -388,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint2 raw[D];
 #pragma unroll
             for (int d = 0; d < D; ++d)
-                if (k1 + d * KS < ke) raw[d] = tc_raw<FMT>(a, nc, k1 + d * KS);
+                if (k1 + d * KS < ke) raw[d] = PRE ? tc_raw_pre<FMT>(a, nc, k1 + d * KS) : tc_raw<FMT>(a, nc, k1 + d * KS);
             for (int kk0 = k1; kk0 < ke && ok; kk0 += D * KS) {
 #pragma unroll
                 for (int d = 0; d < D; ++d) {
@@ -398,8 +466,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int s = gg % kStages, b = gg % kWBufs;
                         const uint32_t ph = (gg / kStages) & 1, phb = (gg / kWBufs) & 1;
                         GroupKey key[4];
-                        tc_keys<FMT>(raw[d], key);
-                        if (k + D * KS < ke) raw[d] = tc_raw<FMT>(a, nc, k + D * KS);
+                        if constexpr (PRE) tc_keys_pre<FMT>(raw[d], key);
+                        else tc_keys<FMT>(raw[d], key);
+                        if (k + D * KS < ke)
+                            raw[d] = PRE ? tc_raw_pre<FMT>(a, nc, k + D * KS) : tc_raw<FMT>(a, nc, k + D * KS);
                         const bool got = mbar_wait_bounded(smem_u32(&sh.full[s]), ph, abort, kWaitNs) &&
                                          mbar_wait_bounded(smem_u32(&sh.wempty[b]), phb ^ 1, abort, kWaitNs);
                         // the tcgen05.st below is warp-collective: decide as a warp
@@ -418,8 +488,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t w[32], w2[32];
                         bool two = false;
                         if constexpr (FMT != kNVFP4) two = __any_sync(0xffffffffu, key[0].two || key[1].two);
-                        if (two) decode_row<FMT, true>(lo, hi, key, w, w2);
-                        else decode_row<FMT, false>(lo, hi, key, w, w2);
+                        if constexpr (PRE) {
+                            if (two) decode_row_pre<FMT, true>(lo, hi, key, w, w2);
+                            else decode_row_pre<FMT, false>(lo, hi, key, w, w2);
+                        } else {
+                            if (two) decode_row<FMT, true>(lo, hi, key, w, w2);
+                            else decode_row<FMT, false>(lo, hi, key, w, w2);
+                        }
                         tmem_st_32x32b_x32(lane_base + kAccCols + b * kWCols, w);
                         if constexpr (FMT == kINT4) tmem_st_32x32b_x32(lane_base + kAccCols + b * kWCols + 32, w2);
                         tmem_wait_st();
@@ -516,10 +591,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int FMT>
+template <int FMT, bool PRE>
 int launch_fmt(const CUtensorMap& ta, const CUtensorMap& tp, const TcArgs& args, dim3 grid, size_t smem,
                cudaStream_t stream) {
-    auto kern = tc_kernel<FMT>;
+    auto kern = tc_kernel<FMT, PRE>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return WQ_ERR_CUDA;
     kern<<<grid, kThreads, smem, stream>>>(ta, tp, args);
@@ -588,6 +663,24 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
         fprintf(stderr, "wq: cuTensorMapEncodeTiled failed (%d): dims %llu x %llu, stride %llu, box %u x %u\n",
                 (int)r, (unsigned long long)inner, (unsigned long long)outer, (unsigned long long)row_bytes,
                 box_inner, box_outer);
+    return r == CUDA_SUCCESS;
+}
+
+// 3-D tiled map, no swizzle: dims / box inner-first, strides of dims 1, 2
+static bool encode_3d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, const uint64_t (&dims)[3],
+                      const uint64_t (&strides)[2], const uint32_t (&box)[3]) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    const cuuint64_t st[2] = {strides[0], strides[1]};
+    const cuuint32_t b[3] = {box[0], box[1], box[2]};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, dt, 3, const_cast<void*>(base), d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS && debug_on())
+        fprintf(stderr, "wq: cuTensorMapEncodeTiled (3-D) failed (%d): dims %llu x %llu x %llu\n", (int)r,
+                (unsigned long long)dims[0], (unsigned long long)dims[1], (unsigned long long)dims[2]);
     return r == CUDA_SUCCESS;
 }
 
@@ -692,31 +785,27 @@ size_t tc_workspace_bytes(int M, int N, int K) {
     return plan_tc(M, N, K, device_sms(), true).ws_bytes;
 }
 
-int launch_tc(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C, int M,
-              int N, int K, int fmt, int group, bool out_f32, void* workspace, size_t workspace_bytes,
-              const Epilogue& epi, cudaStream_t stream) {
-    if (M == 0 || N == 0) return WQ_OK;
-    // shapes this kernel takes: whole k-steps, TMA-legal strides, aligned
-    // scale rows for the per-k-step scale loads
-    if (K <= 0 || K % kBK != 0) return WQ_ERR_UNSUPPORTED;
-    if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(packed) & 15))
-        return WQ_ERR_UNSUPPORTED;
+namespace {
+
+// The launch shared by both weight layouts: tp maps the weight tiles (2-D
+// packed rows, or 3-D prepacked code blocks when pre), scales / zeros are the
+// scale arrays or the record blocks.
+int run_tc(const void* A, const CUtensorMap& tp, bool pre, const uint8_t* scales, const uint8_t* zeros,
+           int kblocks, void* C, int M, int N, int K, int fmt, int group, bool out_f32, void* workspace,
+           size_t workspace_bytes, const Epilogue& epi, cudaStream_t stream) {
     const int sms = device_sms();
     TcPlan plan = plan_tc(M, N, K, sms, workspace != nullptr);
     if (plan.streamk && workspace_bytes < plan.ws_bytes) plan = plan_tc(M, N, K, sms, false);
     const int bm = plan.bm;
     if (!plan.streamk && plan.tiles > 0x7FFFFFFF) return WQ_ERR_UNSUPPORTED;
 
-    CUtensorMap ta, tp;
+    CUtensorMap ta;
     if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kBK, bm,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return WQ_ERR_UNSUPPORTED;
-    if (!encode_2d(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2,
-                   kBK / 2, kBN, CU_TENSOR_MAP_SWIZZLE_32B))
-        return WQ_ERR_UNSUPPORTED;
 
     TcArgs args;
-    args.scales = static_cast<const uint8_t*>(scales);
+    args.scales = scales;
     args.zeros = zeros;
     args.C = C;
     args.ws = nullptr;
@@ -738,17 +827,63 @@ int launch_tc(const void* A, const uint8_t* packed, const void* scales, const ui
     args.nks = plan.nks;
     args.units = plan.units;
     args.G = plan.G;
+    args.kblocks = kblocks;
     args.epi = epi;
     if (debug_on())
-        fprintf(stderr, "wq: tcgen05 M=%d N=%d K=%d: bm=%d tiles=%d %s grid=%d\n", M, N, K, bm, plan.tiles,
-                plan.streamk ? "stream-K" : "data-parallel", plan.G);
+        fprintf(stderr, "wq: tcgen05%s M=%d N=%d K=%d: bm=%d tiles=%d %s grid=%d\n", pre ? " (prepacked)" : "", M, N,
+                K, bm, plan.tiles, plan.streamk ? "stream-K" : "data-parallel", plan.G);
     const dim3 grid(plan.G, 1, 1);
     const size_t smem = 1024 + (size_t)kStages * args.stage_bytes + sizeof(TcShared);
     switch (fmt) {
-        case kNVFP4: return launch_fmt<kNVFP4>(ta, tp, args, grid, smem, stream);
-        case kMXFP4: return launch_fmt<kMXFP4>(ta, tp, args, grid, smem, stream);
-        default: return launch_fmt<kINT4>(ta, tp, args, grid, smem, stream);
+        case kNVFP4:
+            return pre ? launch_fmt<kNVFP4, true>(ta, tp, args, grid, smem, stream)
+                       : launch_fmt<kNVFP4, false>(ta, tp, args, grid, smem, stream);
+        case kMXFP4:
+            return pre ? launch_fmt<kMXFP4, true>(ta, tp, args, grid, smem, stream)
+                       : launch_fmt<kMXFP4, false>(ta, tp, args, grid, smem, stream);
+        default:
+            return pre ? launch_fmt<kINT4, true>(ta, tp, args, grid, smem, stream)
+                       : launch_fmt<kINT4, false>(ta, tp, args, grid, smem, stream);
     }
+}
+
+}  // namespace
+
+int launch_tc(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C, int M,
+              int N, int K, int fmt, int group, bool out_f32, void* workspace, size_t workspace_bytes,
+              const Epilogue& epi, cudaStream_t stream) {
+    if (M == 0 || N == 0) return WQ_OK;
+    // shapes this kernel takes: whole k-steps, TMA-legal strides, aligned
+    // scale rows for the per-k-step scale loads
+    if (K <= 0 || K % kBK != 0) return WQ_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(packed) & 15))
+        return WQ_ERR_UNSUPPORTED;
+    CUtensorMap tp;
+    if (!encode_2d(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2,
+                   kBK / 2, kBN, CU_TENSOR_MAP_SWIZZLE_32B))
+        return WQ_ERR_UNSUPPORTED;
+    return run_tc(A, tp, false, static_cast<const uint8_t*>(scales), zeros, 0, C, M, N, K, fmt, group, out_f32,
+                  workspace, workspace_bytes, epi, stream);
+}
+
+int launch_tc_prepacked(const void* A, const void* prepacked, void* C, int M, int N, int K, int fmt, int group,
+                        bool out_f32, void* workspace, size_t workspace_bytes, const Epilogue& epi,
+                        cudaStream_t stream) {
+    if (M == 0 || N == 0) return WQ_OK;
+    if (K <= 0 || K % kBK != 0) return WQ_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(prepacked) & 15))
+        return WQ_ERR_UNSUPPORTED;
+    const uint64_t I = (uint64_t)(K + 127) / 128, Nb = (uint64_t)(N + 15) / 16;
+    // the code blocks as [Nb][2 I][512 bytes]: one k-step of 128 rows is the
+    // half blocks (ks) of 8 consecutive row blocks, 4 KB
+    CUtensorMap tp;
+    const uint64_t dims[3] = {128, 2 * I, Nb};          // 4-byte elements
+    const uint64_t strides[2] = {512, I * 1024};
+    const uint32_t box[3] = {128, 1, kBN / 16};
+    if (!encode_3d(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT32, prepacked, dims, strides, box)) return WQ_ERR_UNSUPPORTED;
+    const uint8_t* recs = static_cast<const uint8_t*>(prepacked) + Nb * I * 1024;
+    return run_tc(A, tp, true, recs, nullptr, (int)I, C, M, N, K, fmt, group, out_f32, workspace, workspace_bytes,
+                  epi, stream);
 }
 
 }  // namespace wq

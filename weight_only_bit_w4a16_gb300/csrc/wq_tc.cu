@@ -324,8 +324,9 @@ __device__ __forceinline__ bool wait_flag(const unsigned* f, volatile int* abort
 
 // PRE: the weights are in the prepacked layout (tmapP a 3-D map of its code
 // blocks: 512-byte half blocks x 2 per 128-k block x row blocks; scales
-// from its record blocks)
-template <int FMT, bool PRE>
+// from its record blocks).  EPI: the fused epilogue; the plain instance
+// carries no epilogue code at all.
+template <int FMT, bool PRE, bool EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap tmapA, const __grid_constant__ CUtensorMap tmapP, const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -554,13 +555,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         f[4 * j + 3] += t.w;
                     }
                 }
-                // gated: the up row of this gate row is row + 8, held by lane + 8
                 const int mb = m0 + ch * 32;
-                const bool mine = n < a.N && !(a.epi.gated && (row & 8));
+                if constexpr (EPI) {
+                    // gated: the up row of this gate row is row + 8, held by lane + 8
+                    const bool mine = n < a.N && !(a.epi.gated && (row & 8));
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float u = a.epi.gated ? __shfl_xor_sync(0xffffffffu, f[j], 8) : 0.f;
-                    if (mine && mb + j < a.M) store_epilogue(a.epi, a.C, a.out_f32, a.N, mb + j, n, f[j], u);
+                    for (int j = 0; j < 32; ++j) {
+                        const float u = a.epi.gated ? __shfl_xor_sync(0xffffffffu, f[j], 8) : 0.f;
+                        if (mine && mb + j < a.M) store_epilogue(a.epi, a.C, a.out_f32, a.N, mb + j, n, f[j], u);
+                    }
+                } else if (n < a.N) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (mb + j < a.M) {
+                            const size_t o = (size_t)(mb + j) * a.N + n;
+                            if (a.out_f32) static_cast<float*>(a.C)[o] = f[j];
+                            else static_cast<__nv_bfloat16*>(a.C)[o] = __float2bfloat16_rn(f[j]);
+                        }
+                    }
                 }
             }
             // the accumulator may be overwritten by the next segment's MMAs
@@ -594,7 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int FMT, bool PRE>
 int launch_fmt(const CUtensorMap& ta, const CUtensorMap& tp, const TcArgs& args, dim3 grid, size_t smem,
                cudaStream_t stream) {
-    auto kern = tc_kernel<FMT, PRE>;
+    const bool epi = args.epi.bias || args.epi.residual || args.epi.gated;
+    auto kern = epi ? tc_kernel<FMT, PRE, true> : tc_kernel<FMT, PRE, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return WQ_ERR_CUDA;
     kern<<<grid, kThreads, smem, stream>>>(ta, tp, args);

@@ -61,7 +61,9 @@ KERNEL_SOURCES = {  # files whose content defines the dominant kernel of a workl
     "tiny_nvfp4": ["wq_gemv_tma.cu", "wq_gemv.cuh", "wq_common.cuh"],
     "tiny_nvfp4:prepacked": ["wq_gemv_pre.cu", "wq_gemv.cuh", "wq_common.cuh"],
     "prefill_mxfp4": ["wq_tc.cu", "wq_tc.cuh", "wq_common.cuh"],
+    "prefill_mxfp4:prepacked": ["wq_tc.cu", "wq_tc.cuh", "wq_common.cuh"],
     "large_nvfp4": ["wq_tc.cu", "wq_tc.cuh", "wq_common.cuh"],
+    "large_nvfp4:prepacked": ["wq_tc.cu", "wq_tc.cuh", "wq_common.cuh"],
 }
 
 

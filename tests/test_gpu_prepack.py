@@ -344,3 +344,21 @@ def test_auto_route_matches_both_kernels():
     for path in ("auto", "gemv", "tc"):
         C = wq.gemm_prepacked(A, pre, out_dtype="fp32", path=path).cpu().numpy().astype(np.float64)
         assert_parity(C, Ce, S, "fp32", f"route {path}")
+
+
+@pytest.mark.parametrize("layer", ["kv", "down", "lm_head"])
+@pytest.mark.parametrize("M", [1, 16, 128])
+def test_layer_sweep_prepacked(layer, M):
+    """Decoder projections on prepacked weights, the tied LM head (128256 rows,
+    8016 row blocks over the SMs; its prepacked buffer is 207 MB) included:
+    oracle on sampled rows and columns, the calls chained as in decode."""
+    p = synth.layer_problem(layer, M)
+    A, _, _, _ = to_dev(p)
+    pre = prepack_dev(p)
+    C = wq.gemm_prepacked(A, pre, overlap=True).float().cpu().numpy().astype(np.float64)
+    assert wq.wq_get_device_error() == wq.WQ_OK
+    rows, cols = sample(p["M"], 8, 0), sample(p["N"], 48, 1)
+    Ce, S = oracle_ref(p, rows=rows)
+    assert_parity(C[rows], Ce, S, "bf16", f"{layer} M={M} rows")
+    Ce, S = oracle_ref(p, cols=cols)
+    assert_parity(C[:, cols], Ce, S, "bf16", f"{layer} M={M} cols")

@@ -64,7 +64,7 @@ constexpr int kWBufs = 4;       // TMEM weight buffers
 constexpr int kAccCols = kBMMax;  // TMEM columns reserved for the fp32 accumulator
 constexpr int kWCols = kBK;     // TMEM columns per weight buffer: bf16 pairs, hi then lo (int4)
 constexpr int kTmemCols = 512;
-constexpr int kDecodeSets = 2;                      // decode warp sets, alternating k-steps
+constexpr int kDecodeSets = 3;                      // decode warp sets, taking the k-steps in turn
 constexpr int kThreads = 64 + kDecodeSets * 128;    // producer, MMA, decode/epilogue warps
 constexpr int kPTileBytes = kBN * kBK / 2;          // 4 KB of packed weights per stage
 constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s
@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n = n0 + row;
             const int nc = n < a.N ? n : a.N - 1;   // rows past N decode row N-1 (never stored)
             const int g0 = g;
-            const int k1 = kb + ((dset ^ g0) & 1);  // this set's first k-step of the segment
+            const int k1 = kb + ((dset - g0) % KS + KS) % KS;  // this set's first k-step of the segment
             uint2 raw[D];
 #pragma unroll
             for (int d = 0; d < D; ++d)

@@ -362,3 +362,33 @@ def test_layer_sweep_prepacked(layer, M):
     assert_parity(C[rows], Ce, S, "bf16", f"{layer} M={M} rows")
     Ce, S = oracle_ref(p, cols=cols)
     assert_parity(C[:, cols], Ce, S, "bf16", f"{layer} M={M} cols")
+
+
+@pytest.mark.parametrize("fmt,M,N", [("int4", 128, 128256), ("int4", 256, 8192), ("nvfp4", 128, 128256)])
+def test_tc_repeated_calls_bit_identical(fmt, M, N):
+    """The tensor-core kernel is deterministic: every k-step's stage copy is
+    decoded only after it landed, whatever order the copies complete in, so
+    200 repeats of the same call give the same bits (the first checked
+    against the oracle on sampled rows).  The output block is poisoned with
+    NaN before each call, so a store that never happens shows too."""
+    K = 3072
+    p = synth.make_problem(fmt, M, N, K, seed=11)
+    A, _, _, _ = to_dev(p)
+    pre = prepack_dev(p)
+    first = wq.gemm_prepacked(A, pre, path="tc")
+    torch.cuda.synchronize()
+    rows = sample(M, 6, 2)
+    Ce, S = oracle_ref(p, rows=rows)
+    assert_parity(first.float().cpu().numpy().astype(np.float64)[rows], Ce, S, "bf16", f"{fmt} M={M} N={N}")
+    ref = first.view(torch.int16).clone()
+    del first
+    differing = []
+    for r in range(200):
+        torch.full((M, N), float("nan"), device=A.device, dtype=torch.bfloat16)   # freed at once: the next block
+        C = wq.gemm_prepacked(A, pre, path="tc")
+        n_diff = int((C.view(torch.int16) != ref).sum())
+        if n_diff:
+            differing.append((r, n_diff))
+        del C
+    assert wq.wq_get_device_error() == wq.WQ_OK
+    assert not differing, f"{len(differing)}/200 repeats differ from the first (repeat, elements): {differing[:8]}"

@@ -483,8 +483,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         else tc_keys<FMT>(raw[d], key);
                         if (k + D * KS < ke)
                             raw[d] = PRE ? tc_raw_pre<FMT>(a, nc, k + D * KS) : tc_raw<FMT>(a, nc, k + D * KS);
-                        const bool got = mbar_wait_bounded(smem_u32(&sh.full[s]), ph, abort, kWaitNs) &&
-                                         mbar_wait_bounded(smem_u32(&sh.wempty[b]), phb ^ 1, abort, kWaitNs);
+                        // Weight buffer first, stage second.  A set never waits on
+                        // the stage phase of k-step gg - kStages (another set's), so
+                        // on its own the parity test on full[s] could match that
+                        // older phase when copies land out of order, and the decode
+                        // would read the stage before this k-step's copy.  The MMA
+                        // of k-step gg - kWBufs has consumed every copy up to it,
+                        // that of gg - kStages included, so the full[s] wait after
+                        // it can only match this k-step's phase.
+                        static_assert(kWBufs <= kStages, "the weight-buffer wait must imply the older stage phase");
+                        const bool got = mbar_wait_bounded(smem_u32(&sh.wempty[b]), phb ^ 1, abort, kWaitNs) &&
+                                         mbar_wait_bounded(smem_u32(&sh.full[s]), ph, abort, kWaitNs);
                         // the tcgen05.st below is warp-collective: decide as a warp
                         if (!__all_sync(0xffffffffu, got)) {
                             if (!got) record_timeout();
@@ -508,9 +517,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (two) decode_row<FMT, true>(lo, hi, key, w, w2);
                             else decode_row<FMT, false>(lo, hi, key, w, w2);
                         }
-                        tmem_st_32x32b_x32(lane_base + kAccCols + b * kWCols, w);
-                        if constexpr (FMT == kINT4) tmem_st_32x32b_x32(lane_base + kAccCols + b * kWCols + 32, w2);
-                        tmem_wait_st();
+                        if constexpr (FMT == kINT4)
+                            tmem_st2_32x32b_x32_sync(lane_base + kAccCols + b * kWCols, w,
+                                                     lane_base + kAccCols + b * kWCols + 32, w2);
+                        else
+                            tmem_st_32x32b_x32_sync(lane_base + kAccCols + b * kWCols, w);
                         tc_fence_before();
                         mbar_arrive(smem_u32(&sh.wfull[b]));
                     }
@@ -541,11 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int ch = dset; ch < a.bm / 32; ch += kDecodeSets) {
                 uint32_t v[32];
-                if (ok) {
-                    tmem_ld_32x32b_x32(lane_base + ch * 32, v);
-                    tmem_wait_ld();
-                }
                 if (!ok) continue;
+                tmem_ld_32x32b_x32_sync(lane_base + ch * 32, v);
                 if (!owner) {
                     // a tile this CTA starts but does not end: its partial sums
 #pragma unroll

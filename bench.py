@@ -529,40 +529,53 @@ def fused_gate_up(w, dev, l2):
 def run_e2e(args, w, A_by_M, weights, pool, dev, ws, pre_pool=None):
     """The same metric through the public API (weight_only_bit_w4a16_gb300.gemm,
     or gemm_prepacked on prepacked weights) from pinned host memory.  Per
-    step: H2D of each call's activations, the calls on device-resident
-    weights (uploaded -- and repacked -- once, as a model's weights are), D2H
-    of each result.  A second figure also uploads the weights every step
-    (and repacks them, for the prepacked layout)."""
+    step: one H2D copy of the step's activations (all its calls' A, packed
+    in one pinned buffer), the calls chained on device-resident weights
+    (uploaded -- and repacked -- once, as a model's weights are), one D2H
+    copy of all the step's results.  A second figure also uploads the
+    weights every step (and repacks them, for the prepacked layout)."""
     import torch
     import weight_only_bit_w4a16_gb300 as wq
     from weight_only_bit_w4a16_gb300 import metrics
     fmt, group, Ms, N, K, out = w["fmt"], w["group"], w["Ms"], w["N"], w["K"], w["out"]
     odt = torch.float32 if out == "fp32" else torch.bfloat16
-    A_h = {M: torch.from_numpy(A_by_M[M].view(np.int16)).view(torch.bfloat16).pin_memory() for M in Ms}
-    C_h = {M: torch.empty((M, N), dtype=odt).pin_memory() for M in Ms}
-    A_d = {M: torch.empty((M, K), dtype=torch.bfloat16, device=dev) for M in Ms}
-    C_d = {M: torch.empty((M, N), dtype=odt, device=dev) for M in Ms}
+    # one pinned host buffer and one device buffer for all of a step's
+    # activations, and likewise for its results; per-call views into them
+    a_rows, c_rows = sum(Ms), sum(Ms)
+    A_h_all = torch.empty((a_rows, K), dtype=torch.bfloat16).pin_memory()
+    C_h_all = torch.empty((c_rows, N), dtype=odt).pin_memory()
+    A_d_all = torch.empty((a_rows, K), dtype=torch.bfloat16, device=dev)
+    C_d_all = torch.empty((c_rows, N), dtype=odt, device=dev)
+    A_d, C_d, r0 = {}, {}, 0
+    for M in Ms:
+        A_h_all[r0:r0 + M].copy_(torch.from_numpy(A_by_M[M].view(np.int16)).view(torch.bfloat16))
+        A_d[M], C_d[M] = A_d_all[r0:r0 + M], C_d_all[r0:r0 + M]
+        r0 += M
     s = torch.cuda.Stream(dev)
     R = len(pool)
     steps = max(1, min(args.steps, 2000))
+    overlap = not args.no_overlap
 
     def one(i, upload_weights=None):
-        for j, M in enumerate(Ms):
-            slot = (i * len(Ms) + j) % R
-            pk, sc, zr = pool[slot]
-            if upload_weights is not None:
+        if upload_weights is not None:
+            for j, M in enumerate(Ms):
+                slot = (i * len(Ms) + j) % R
+                pk, sc, zr = pool[slot]
                 pk.copy_(upload_weights[0], non_blocking=True)
                 sc.copy_(upload_weights[1], non_blocking=True)
                 if zr is not None:
                     zr.copy_(upload_weights[2], non_blocking=True)
                 if pre_pool is not None:
                     wq.prepack(pk, sc, zr, fmt, group, out=pre_pool[slot].buf)
-            A_d[M].copy_(A_h[M], non_blocking=True)
+        A_d_all.copy_(A_h_all, non_blocking=True)
+        for j, M in enumerate(Ms):
+            slot = (i * len(Ms) + j) % R
             if pre_pool is not None:
-                wq.gemm_prepacked(A_d[M], pre_pool[slot], out_dtype=out, out=C_d[M])
+                wq.gemm_prepacked(A_d[M], pre_pool[slot], out_dtype=out, out=C_d[M], overlap=overlap and j > 0)
             else:
-                wq.gemm(A_d[M], pk, sc, zr, fmt, group, out_dtype=out, out=C_d[M])
-            C_h[M].copy_(C_d[M], non_blocking=True)
+                pk, sc, zr = pool[slot]
+                wq.gemm(A_d[M], pk, sc, zr, fmt, group, out_dtype=out, out=C_d[M], overlap=overlap and j > 0)
+        C_h_all.copy_(C_d_all, non_blocking=True)
 
     def timed(nsteps, upload=None):
         with torch.cuda.stream(s):
@@ -579,8 +592,8 @@ def run_e2e(args, w, A_by_M, weights, pool, dev, ws, pre_pool=None):
         torch.cuda.synchronize()
         return max_over_ranks(e0.elapsed_time(e1), dev)
 
-    h2d = sum(A_h[M].numel() * 2 for M in Ms)
-    d2h = sum(C_h[M].numel() * C_h[M].element_size() for M in Ms)
+    h2d = A_h_all.numel() * 2
+    d2h = C_h_all.numel() * C_h_all.element_size()
     ms = timed(steps)
     wbytes = metrics.weight_bytes(fmt, N, K, group)
     if w["unit"] == "GB/s":

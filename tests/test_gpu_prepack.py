@@ -14,7 +14,7 @@ from oracle import prepack as opk
 import weight_only_bit_w4a16_gb300 as wq
 from weight_only_bit_w4a16_gb300 import synth
 
-from gpu_util import assert_parity, oracle_ref, sample, to_dev
+from gpu_util import assert_parity, host_rows_cols, oracle_ref, sample, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -346,22 +346,26 @@ def test_auto_route_matches_both_kernels():
         assert_parity(C, Ce, S, "fp32", f"route {path}")
 
 
-@pytest.mark.parametrize("layer", ["kv", "down", "lm_head"])
-@pytest.mark.parametrize("M", [1, 16, 128])
+@pytest.mark.parametrize("layer", list(synth.LAYER_SHAPES))
+@pytest.mark.parametrize("M", [1, 16, 128, 2048])
 def test_layer_sweep_prepacked(layer, M):
-    """Decoder projections on prepacked weights, the tied LM head (128256 rows,
-    8016 row blocks over the SMs; its prepacked buffer is 207 MB) included:
-    oracle on sampled rows and columns, the calls chained as in decode."""
+    """Every decoder projection on prepacked weights at every M, the tied LM
+    head (128256 rows, 8016 row blocks over the SMs; its prepacked buffer is
+    207 MB, its M = 2048 output 0.5 GB) included: oracle on sampled rows and
+    columns, copied from the device alone, the calls chained as in decode."""
     p = synth.layer_problem(layer, M)
     A, _, _, _ = to_dev(p)
     pre = prepack_dev(p)
-    C = wq.gemm_prepacked(A, pre, overlap=True).float().cpu().numpy().astype(np.float64)
+    C = wq.gemm_prepacked(A, pre, overlap=True)
+    torch.cuda.synchronize()
     assert wq.wq_get_device_error() == wq.WQ_OK
     rows, cols = sample(p["M"], 8, 0), sample(p["N"], 48, 1)
+    Cr, Cc = host_rows_cols(C, rows, cols)
+    del C, pre
     Ce, S = oracle_ref(p, rows=rows)
-    assert_parity(C[rows], Ce, S, "bf16", f"{layer} M={M} rows")
+    assert_parity(Cr, Ce, S, "bf16", f"{layer} M={M} rows")
     Ce, S = oracle_ref(p, cols=cols)
-    assert_parity(C[:, cols], Ce, S, "bf16", f"{layer} M={M} cols")
+    assert_parity(Cc, Ce, S, "bf16", f"{layer} M={M} cols")
 
 
 @pytest.mark.parametrize("fmt,M,N", [("int4", 128, 128256), ("int4", 256, 8192), ("nvfp4", 128, 128256)])
@@ -392,3 +396,50 @@ def test_tc_repeated_calls_bit_identical(fmt, M, N):
         del C
     assert wq.wq_get_device_error() == wq.WQ_OK
     assert not differing, f"{len(differing)}/200 repeats differ from the first (repeat, elements): {differing[:8]}"
+
+
+# -- fp4 tiles of more than 256 activation rows: two MMAs on one decode -------------
+@pytest.mark.parametrize("bm", [288, 320, 352, 384])
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("layout", ["plain", "prepacked"])
+def test_tc_two_mma_tiles(fmt, bm, layout, monkeypatch):
+    """Tile heights above one MMA's 256 rows (forced): the second MMA's
+    activation box is ragged (M = bm - 40), wholly past M (M = bm / 2 - 8),
+    or the start of a second, ragged m-tile (M = 2 bm - 8).  N spans three
+    weight tiles, the last ragged; K nine k-steps."""
+    monkeypatch.setenv("WQ_TC_BM", str(bm))
+    for M in (bm - 40, bm // 2 - 8, 2 * bm - 8):
+        p = synth.make_problem(fmt, M, 300, 576, seed=bm + M)
+        if layout == "prepacked":
+            C = run_tc(p, "fp32")
+        else:
+            from gpu_util import gpu_gemm
+            C = gpu_gemm(p, "fp32", path="tc")
+        Ce, S = oracle_ref(p)
+        assert_parity(C, Ce, S, "fp32", f"{fmt} bm={bm} M={M} {layout}")
+
+
+def test_tc_two_mma_tiles_fused_epilogue(monkeypatch):
+    """The fused epilogue (bias, SiLU-gated pairs, residual) on a 320-row tile."""
+    monkeypatch.setenv("WQ_TC_BM", "320")
+    M = 600
+    p = synth.make_problem("nvfp4", M, 256, 1024, seed=78)
+    rng = np.random.default_rng(M)
+    bias = synth.bf16_bits((rng.normal(size=256) * 0.5).astype(np.float32))
+    res = synth.bf16_bits(rng.normal(size=(M, 128)).astype(np.float32))
+    dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    Y = run_tc(p, "bf16", bias=dev(bias), residual=dev(res), gated=True)
+    C, S = oracle.gemm(p["A"], p["packed"], p["scales"], p["zeros"], "nvfp4", 16)
+    Ye, T = oracle.epilogue(C, S, bias, res, True, "bf16")
+    assert not (np.abs(Y - Ye) > T).any()
+
+
+def test_tc_int4_keeps_256_rows(monkeypatch):
+    """int4 tiles stay within one MMA (its hi and lo weight buffers take the
+    TMEM columns a second accumulator half would need): a forced height
+    above 256 falls back to the default choice and the result holds."""
+    monkeypatch.setenv("WQ_TC_BM", "320")
+    p = synth.make_problem("int4", 400, 256, 1024, seed=79)
+    C = run_tc(p, "fp32")
+    Ce, S = oracle_ref(p)
+    assert_parity(C, Ce, S, "fp32", "int4 forced 320")

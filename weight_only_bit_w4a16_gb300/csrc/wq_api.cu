@@ -103,7 +103,8 @@ WQ_EXPORT int wq_gemm_static(const void* A, const uint8_t* packed, const void* s
         const size_t v = (size_t)strtoull(e, nullptr, 10);
         if (v < cap) cap = v;
     }
-    const size_t need = (M > 16 && N > 0 && K > 0 && K % 64 == 0) ? wq::tc_workspace_bytes(M, N, K) : 0;
+    const size_t need =
+        (M > 16 && N > 0 && K > 0 && K % 64 == 0) ? wq::tc_workspace_bytes(M, N, K, format & 0xFF) : 0;
     if (need > cap) return WQ_ERR_UNSUPPORTED;
     return gemm_impl(A, packed, scales, zeros, C, M, N, K, format, group, ws, cap, stream, path);
 }
@@ -121,7 +122,7 @@ WQ_EXPORT size_t wq_gemm_workspace_size(int M, int N, int K, int format, int gro
                       (format & 0xFF) == WQ_INT4 ? reinterpret_cast<const uint8_t*>(16) : nullptr, N, K,
                       format & 0xFF, group) != WQ_OK)
         return 0;
-    return wq::tc_workspace_bytes(M, N, K);
+    return wq::tc_workspace_bytes(M, N, K, format & 0xFF);
 }
 
 WQ_EXPORT int wq_gemm(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C, int M,

@@ -35,7 +35,7 @@ int launch_gemv_tma(const void* A, const uint8_t* packed, const void* scales, co
 int launch_tc(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
               void* C, int M, int N, int K, int fmt, int group, bool out_f32, void* workspace,
               size_t workspace_bytes, const Epilogue& epi, cudaStream_t stream);
-size_t tc_workspace_bytes(int M, int N, int K);
+size_t tc_workspace_bytes(int M, int N, int K, int fmt);
 
 // The tensor-core kernel on prepacked weights (same contract as launch_tc;
 // one k-step of 128 rows is 8 row blocks' half blocks).

@@ -3,15 +3,15 @@
 // its bounded waits report into.
 //
 // Tile: 128 weight rows (n) x bm activation rows (m, a multiple of 32 up to
-// 256, chosen per call to limit the last partial wave) x all of K, in
-// k-steps of 64.  The product is computed transposed, D = W . A^T, so that
-// the dequantised weights are the A operand of tcgen05.mma and can live in
-// TMEM:
+// 256 for int4 and 384 for the fp4 formats, chosen per call to limit the
+// last partial wave) x all of K, in k-steps of 64.  The product is computed
+// transposed, D = W . A^T, so that the dequantised weights are the A operand
+// of tcgen05.mma and can live in TMEM:
 //   * warp 0, one lane: TMA producer.  Per k-step it loads the activation
 //     tile (bm x 64 bf16, 128-byte swizzle, the MMA's B operand in shared
-//     memory) and the packed weight tile (128 rows x 32 bytes, 32-byte
-//     swizzle) into a ring of kStages stages, completing on the stage's
-//     "full" mbarrier.
+//     memory; above 256 rows as two boxes of bm / 2) and the packed weight
+//     tile (128 rows x 32 bytes, 32-byte swizzle) into a ring of kStages
+//     stages, completing on the stage's "full" mbarrier.
 //   * warps 2.. (kDecodeSets sets of 4 warps, thread = weight row; set j
 //     takes the k-steps ks = j mod kDecodeSets): decode.  Each thread reads
 //     its row's 32 packed bytes, dequantises them in registers (the routine
@@ -22,7 +22,11 @@
 //   * warp 1, one lane: issues 4 (int4: 8) tcgen05.mma.kind::f16 (M=128,
 //     N=bm, K=16) per k-step with A from TMEM, B from shared memory, the
 //     fp32 accumulator in TMEM; tcgen05.commit frees the stage and the TMEM
-//     weight buffer.
+//     weight buffer.  Above 256 rows (fp4) the tile is two MMAs of N = bm / 2
+//     on the same decoded weights: one decode of a k-step feeds up to 384
+//     activation rows.  This is what the fp4 weight buffers' 32 TMEM columns
+//     leave room for (384 accumulator + 4 x 32 = 512 columns); int4 keeps
+//     256 + 4 x 64 (its hi and lo terms).
 //   * the decode warps again: epilogue, tcgen05.ld of the accumulator (their
 //     lane quarter; the sets split the columns), fp32 -> bf16/fp32, stores.
 // Every wait is bounded in wall time (%globaltimer); a wait that runs out
@@ -57,20 +61,25 @@ namespace {
 using namespace sm100;
 
 constexpr int kBN = 128;        // weight rows per tile (MMA M)
-constexpr int kBMMax = 256;     // activation rows per tile (MMA N): a multiple of 32, <= 256
+constexpr int kBMMax = 256;     // activation rows of one MMA (its N), of an int4 tile and of a stream-K tile
+constexpr int kBMMaxFp4 = 384;  // activation rows of an fp4 data-parallel tile: two MMAs of N = bm / 2
 constexpr int kBK = 64;         // k per stage
 constexpr int kStages = 4;
 constexpr int kWBufs = 4;       // TMEM weight buffers
-constexpr int kAccCols = kBMMax;  // TMEM columns reserved for the fp32 accumulator
-constexpr int kWCols = kBK;     // TMEM columns per weight buffer: bf16 pairs, hi then lo (int4)
 constexpr int kTmemCols = 512;
+// TMEM columns per weight buffer (bf16 pairs of a row's 64 weights: int4 hi
+// then lo, fp4 the weights alone) and the fp32 accumulator's columns before them
+template <int FMT>
+constexpr int kWColsOf = FMT == kINT4 ? 2 * kBK / 2 : kBK / 2;
+template <int FMT>
+constexpr int kAccColsOf = kTmemCols - kWBufs * kWColsOf<FMT>;
+static_assert(kAccColsOf<kINT4> >= kBMMax && kAccColsOf<kNVFP4> >= kBMMaxFp4, "TMEM budget");
 constexpr int kDecodeSets = 3;                      // decode warp sets, taking the k-steps in turn
 constexpr int kThreads = 64 + kDecodeSets * 128;    // producer, MMA, decode/epilogue warps
 constexpr int kPTileBytes = kBN * kBK / 2;          // 4 KB of packed weights per stage
 constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s
 constexpr uint64_t kDrainNs = 100000000ull;        // 0.1 s
 
-static_assert(kAccCols + kWBufs * kWCols <= kTmemCols, "TMEM budget");
 
 struct TcArgs {
     const uint8_t* scales;   // prepacked weights: the record blocks
@@ -80,10 +89,11 @@ struct TcArgs {
     unsigned* flags;    // stream-K "partial of CTA c is ready" flags [G], zero between calls
     int M, N, K, group;
     int out_f32;
-    int bm;             // activation rows per tile (MMA N), a multiple of 32
+    int bm;             // activation rows per tile, a multiple of 32
+    int bh;             // activation rows per MMA and per TMA box: bm, or bm / 2 above kBMMax
     int a_tile_bytes;   // bm * 128: the activation tile of a stage
     int stage_bytes;    // a_tile_bytes + packed tile; a multiple of 1024 (128-byte swizzle period)
-    uint32_t idesc;     // instruction descriptor: M = 128, N = bm
+    uint32_t idesc;     // instruction descriptor: M = 128, N = bh
     int nt_n;           // tiles along N; tile t covers rows (t % nt_n) * 128, activations (t / nt_n) * bm
     int nks;            // k-steps per tile
     long long units;    // tiles * nks
@@ -337,10 +347,14 @@ __device__ __forceinline__ bool wait_flag(const unsigned* f, volatile int* abort
 // PRE: the weights are in the prepacked layout (tmapP a 3-D map of its code
 // blocks: 512-byte half blocks x 2 per 128-k block x row blocks; scales
 // from its record blocks).  EPI: the fused epilogue; the plain instance
-// carries no epilogue code at all.
-template <int FMT, bool PRE, bool EPI>
+// carries no epilogue code at all.  SPLIT (fp4): tiles of bm = 2 bh rows, two
+// MMAs per 16-k slice.  It is a template parameter, not a runtime test: a
+// never-taken branch around the second MMA in the issuing loop cost the
+// one-MMA tiles 27 % (8192^3 NVFP4 prepacked, same GPU: 776 -> 983 us).
+template <int FMT, bool PRE, bool EPI, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap tmapA, const __grid_constant__ CUtensorMap tmapP, const TcArgs a) {
+    static_assert(!(SPLIT && FMT == kINT4), "int4 tiles use one MMA per slice and its residual");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // stages 1024-byte aligned (the 128-byte swizzle pattern repeats every 1 KB)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -398,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb = smem_u32(&sh.full[s]);
                     mbar_arrive_expect_tx(fb, kStageBytes);
                     tma_load_2d(smem_u32(st), &tmapA, fb, k * kBK, m0);
+                    if constexpr (SPLIT) tma_load_2d(smem_u32(st + a.bh * 128), &tmapA, fb, k * kBK, m0 + a.bh);
                     if constexpr (PRE) tma_load_3d(smem_u32(st + kATileBytes), &tmapP, fb, 0, k, n0 >> 4);
                     else tma_load_2d(smem_u32(st + kATileBytes), &tmapP, fb, k * (kBK / 2), n0);
                 }
@@ -432,9 +447,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint64_t bdesc = smem_desc_sw128_kmajor(a_addr + kk * 32);
-                        const uint32_t wcol = tmem + kAccCols + b * kWCols + kk * 8;
-                        mma_ts_f16(tmem, wcol, bdesc, a.idesc, (k != kb || kk != 0) ? 1u : 0u);
-                        if constexpr (FMT == kINT4) mma_ts_f16(tmem, wcol + 32, bdesc, a.idesc, 1);   // the residual
+                        const uint32_t wcol = tmem + kAccColsOf<FMT> + b * kWColsOf<FMT> + kk * 8;
+                        const uint32_t acc = (k != kb || kk != 0) ? 1u : 0u;
+                        mma_ts_f16(tmem, wcol, bdesc, a.idesc, acc);
+                        if constexpr (FMT == kINT4) {
+                            mma_ts_f16(tmem, wcol + 32, bdesc, a.idesc, 1);   // the residual
+                        } else if constexpr (SPLIT) {
+                            // the tile's second half: the same weights, activation
+                            // rows bh.., accumulator columns bh..
+                            mma_ts_f16(tmem + a.bh, wcol, smem_desc_sw128_kmajor(a_addr + a.bh * 128 + kk * 32),
+                                       a.idesc, acc);
+                        }
                     }
                     tc_commit(smem_u32(&sh.empty[s]));
                     tc_commit(smem_u32(&sh.wempty[b]));
@@ -517,11 +540,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (two) decode_row<FMT, true>(lo, hi, key, w, w2);
                             else decode_row<FMT, false>(lo, hi, key, w, w2);
                         }
+                        const uint32_t wbuf = lane_base + kAccColsOf<FMT> + b * kWColsOf<FMT>;
                         if constexpr (FMT == kINT4)
-                            tmem_st2_32x32b_x32_sync(lane_base + kAccCols + b * kWCols, w,
-                                                     lane_base + kAccCols + b * kWCols + 32, w2);
+                            tmem_st2_32x32b_x32_sync(wbuf, w, wbuf + 32, w2);
                         else
-                            tmem_st_32x32b_x32_sync(lane_base + kAccCols + b * kWCols, w);
+                            tmem_st_32x32b_x32_sync(wbuf, w);
                         tc_fence_before();
                         mbar_arrive(smem_u32(&sh.wfull[b]));
                     }
@@ -627,7 +650,10 @@ template <int FMT, bool PRE>
 int launch_fmt(const CUtensorMap& ta, const CUtensorMap& tp, const TcArgs& args, dim3 grid, size_t smem,
                cudaStream_t stream) {
     const bool epi = args.epi.bias || args.epi.residual || args.epi.gated;
-    auto kern = epi ? tc_kernel<FMT, PRE, true> : tc_kernel<FMT, PRE, false>;
+    auto kern = epi ? tc_kernel<FMT, PRE, true, false> : tc_kernel<FMT, PRE, false, false>;
+    if constexpr (FMT != kINT4) {
+        if (args.bh < args.bm) kern = epi ? tc_kernel<FMT, PRE, true, true> : tc_kernel<FMT, PRE, false, true>;
+    }
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return WQ_ERR_CUDA;
     kern<<<grid, kThreads, smem, stream>>>(ta, tp, args);
@@ -731,26 +757,49 @@ int device_sms() {
     return sms;
 }
 
-// Tile height (MMA N) for M activation rows.  Data-parallel: fewest waves of
-// one-CTA-per-SM tiles, each costing about (bm + 64) -- MMA time grows with
-// bm, the decode of a k-step does not.  Stream-K: least total work,
-// tiles x (bm + 64), as the CTAs share it evenly.
-int choose_bm(int M, int N, int sms, bool streamk) {
+// Cycles of one k-step of an fp4 data-parallel tile of bm rows, measured on
+// the prepacked layout (8192^3 NVFP4 and 2048 x 3072^2 MXFP4, 2070 MHz): one
+// MMA is decode-bound at ~896 cycles up to 256 rows (its own time, ~2.6 per
+// row, stays below that); two MMAs on one decode cost ~3.67 per row (1180 at
+// 320 rows, ~1290 at 352).
+long long fp4_kstep_cycles(int bm) {
+    return bm <= kBMMax ? (896 > 26 * bm / 10 ? 896 : 26 * bm / 10) : 367LL * bm / 100;
+}
+
+// Tile height (activation rows) for M rows.  Data-parallel: least time, the
+// waves of one-CTA-per-SM tiles times a tile's k-step cost -- for int4 about
+// (bm + 64) (MMA time grows with bm, the decode of a k-step does not), for
+// the fp4 formats fp4_kstep_cycles, up to 384 rows (two MMAs on one decode,
+// chosen where they save enough waves: the 2048 x 3072 x 3072 prefill runs 144
+// tiles of 352 rows in one wave instead of 264 of 192 in two).  Stream-K:
+// least total work, tiles x (bm + 64), as the CTAs share it evenly, up to 256
+// rows.
+int choose_bm(int M, int N, int sms, bool streamk, int fmt) {
     const int nt = (N + kBN - 1) / kBN;
+    const int bm_max = (fmt != kINT4 && !streamk) ? kBMMaxFp4 : kBMMax;
     int bm = 0;
     long long best = -1;
-    for (int cand = kBMMax; cand >= 32; cand -= 32) {
+    for (int cand = bm_max; cand >= 32; cand -= 32) {
         if (cand < 128 && cand < ((M + 31) / 32) * 32) continue;   // small tiles only to fit a small M
         const long long tiles = (long long)nt * ((M + cand - 1) / cand);
-        const long long cost = streamk ? tiles * (cand + 64) : ((tiles + sms - 1) / sms) * (cand + 64);
-        if (best < 0 || cost < best) {
+        const long long waves = (tiles + sms - 1) / sms;
+        const long long cost = streamk ? tiles * (cand + 64)
+                               : fmt == kINT4 ? waves * (cand + 64)
+                                              : waves * fp4_kstep_cycles(cand);
+        // candidates run from tall to short.  On a tie of the fp4 model (the
+        // same waves of decode-bound one-MMA tiles) the shorter tile wins: the
+        // same time, fewer padded rows.  The int4 and stream-K models keep the
+        // taller tile (2048 x 8192 x 3072 int4: 4 waves of 256 rows run 122 us,
+        // 5 of 192 rows 142 us, which the (bm + 64) model scores alike).
+        const bool fp4_dp = fmt != kINT4 && !streamk;
+        if (best < 0 || cost < best || (fp4_dp && cost == best)) {
             best = cost;
             bm = cand;
         }
     }
     if (const char* e = getenv("WQ_TC_BM")) {
         const int v = atoi(e);
-        if (v >= 32 && v <= kBMMax && v % 32 == 0) bm = v;
+        if (v >= 32 && v <= bm_max && v % 32 == 0) bm = v;
     }
     return bm;
 }
@@ -764,7 +813,7 @@ struct TcPlan {
 
 constexpr size_t kFlagBytes(int G) { return ((size_t)G * sizeof(unsigned) + 255) / 256 * 256; }
 
-TcPlan plan_tc(int M, int N, int K, int sms, bool allow_streamk) {
+TcPlan plan_tc(int M, int N, int K, int sms, bool allow_streamk, int fmt) {
     TcPlan p{};
     p.nks = K / kBK;
     p.nt_n = (N + kBN - 1) / kBN;
@@ -773,13 +822,13 @@ TcPlan plan_tc(int M, int N, int K, int sms, bool allow_streamk) {
     // out, partials in) costs more than the idle SMs (measured: 2048 x 3072 x
     // 3072 runs 87% full on whole tiles and is faster that way; 128 x 3072 x
     // 3072 -- 24 tiles on 152 SMs -- runs 1.8x faster split)
-    int bm = choose_bm(M, N, sms, false);
+    int bm = choose_bm(M, N, sms, false, fmt);
     long long tiles = (long long)p.nt_n * ((M + bm - 1) / bm);
     const long long waves = (tiles + sms - 1) / sms;
     bool sk = allow_streamk && (double)tiles / (double)(waves * sms) < 0.75;
     if (allow_streamk && getenv("WQ_TC_STREAMK")) sk = atoi(getenv("WQ_TC_STREAMK")) != 0;   // tests, tuning
     if (sk) {
-        bm = choose_bm(M, N, sms, true);
+        bm = choose_bm(M, N, sms, true, fmt);
         tiles = (long long)p.nt_n * ((M + bm - 1) / bm);
     }
     p.bm = bm;
@@ -813,9 +862,9 @@ void* static_workspace(size_t* bytes) {
     return addr[dev];
 }
 
-size_t tc_workspace_bytes(int M, int N, int K) {
+size_t tc_workspace_bytes(int M, int N, int K, int fmt) {
     if (M <= 0 || N <= 0 || K <= 0 || K % kBK != 0) return 0;
-    return plan_tc(M, N, K, device_sms(), true).ws_bytes;
+    return plan_tc(M, N, K, device_sms(), true, fmt).ws_bytes;
 }
 
 namespace {
@@ -827,13 +876,15 @@ int run_tc(const void* A, const CUtensorMap& tp, bool pre, const uint8_t* scales
            int kblocks, void* C, int M, int N, int K, int fmt, int group, bool out_f32, void* workspace,
            size_t workspace_bytes, const Epilogue& epi, cudaStream_t stream) {
     const int sms = device_sms();
-    TcPlan plan = plan_tc(M, N, K, sms, workspace != nullptr);
-    if (plan.streamk && workspace_bytes < plan.ws_bytes) plan = plan_tc(M, N, K, sms, false);
+    TcPlan plan = plan_tc(M, N, K, sms, workspace != nullptr, fmt);
+    if (plan.streamk && workspace_bytes < plan.ws_bytes) plan = plan_tc(M, N, K, sms, false, fmt);
     const int bm = plan.bm;
+    const int bh = bm > kBMMax ? bm / 2 : bm;   // rows of one MMA and one TMA box
+    if (bm > kBMMax && (fmt == kINT4 || plan.streamk || bh % 16 != 0)) return WQ_ERR_UNSUPPORTED;
     if (!plan.streamk && plan.tiles > 0x7FFFFFFF) return WQ_ERR_UNSUPPORTED;
 
     CUtensorMap ta;
-    if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kBK, bm,
+    if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kBK, bh,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return WQ_ERR_UNSUPPORTED;
 
@@ -853,9 +904,10 @@ int run_tc(const void* A, const CUtensorMap& tp, bool pre, const uint8_t* scales
     args.group = group;
     args.out_f32 = out_f32 ? 1 : 0;
     args.bm = bm;
+    args.bh = bh;
     args.a_tile_bytes = bm * kBK * 2;
     args.stage_bytes = args.a_tile_bytes + kPTileBytes;
-    args.idesc = idesc_bf16_f32(kBN, bm);
+    args.idesc = idesc_bf16_f32(kBN, bh);
     args.nt_n = plan.nt_n;
     args.nks = plan.nks;
     args.units = plan.units;

@@ -2,7 +2,7 @@
 """Benchmark of the GB300 W4A16 dequantise-GEMM library.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode_int4|prefill_mxfp4|large_nvfp4|tiny_nvfp4]
+                    [--workload decode_int4|prefill_mxfp4|large_nvfp4|tiny_nvfp4|layer_sweep]
 
 Default workload (decode_int4): the decode GEMV of the 3B int4-g128 model's
 gate/up projection, N=8192, K=3072, bf16 activations, bf16 output.  One STEP
@@ -19,6 +19,12 @@ metric, value, unit, roofline (dominant kernel, live CUDA-event timing),
 cpu_baseline (the oracle on the host cores, bounded sample), e2e (through the
 public Python API with pinned host buffers), clocks (nvidia-smi sampled
 during the timed region), gpu_launches.
+
+--workload layer_sweep: one step is every projection of the 3B decoder (q,
+k, v, o, gate, up, down) and the tied LM head, int4 g128, at M = 1, 16, 128
+and 2048 (32 chained calls); the value is the step's fraction of the roofline
+(sum over the calls of max(bytes / HBM, flops / bf16 tensor peak) over the
+measured step time), with every (shape, M) also timed alone in "per_shape".
 
 --impl reference times the oracle (the fp64 CPU implementation under
 oracle/) on the same workload and prints the same line with
@@ -53,7 +59,17 @@ BENCH_WORKLOADS = {
                         bound="tensor", metric="dequant-GEMM TFLOP/s (large M)", unit="TFLOP/s"),
     "tiny_nvfp4": dict(fmt="nvfp4", group=16, Ms=(16,), N=256, K=512, out="fp32",
                        bound="hbm", metric="weight HBM GB/s (M≤16)", unit="GB/s"),
+    # every projection of the 3B decoder (k and v, gate and up: two calls of
+    # one shape, distinct weights) and the tied LM head, at M = 1, 16, 128,
+    # 2048; one step is all 32 calls, chained; the value is the step's
+    # fraction of the roofline: sum over calls of max(bytes / HBM, flops /
+    # tensor peak), over the measured step time
+    "layer_sweep": dict(fmt="int4", group=128, Ms=(1, 16, 128, 2048), out="bf16", bound="roofline",
+                        calls=(("q", "q"), ("k", "kv"), ("v", "kv"), ("o", "o"), ("gate", "gate_up"),
+                               ("up", "gate_up"), ("down", "down"), ("lm_head", "lm_head")),
+                        metric="% of roofline (decoder-layer sweep)", unit="% of roofline"),
 }
+DEFAULT_STEPS = {"layer_sweep": (300, 10)}   # (steps, warm-up) when not given: one step is ~2 ms
 
 KERNEL_SOURCES = {  # files whose content defines the dominant kernel of a workload (and layout)
     "decode_int4": ["wq_gemv_tma.cu", "wq_gemv.cuh", "wq_common.cuh"],
@@ -660,11 +676,360 @@ def run_reference(args):
     print(json.dumps(res), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# the decoder-layer sweep
+# ---------------------------------------------------------------------------
+def sweep_shapes(w):
+    from weight_only_bit_w4a16_gb300 import synth
+    return {c: synth.LAYER_SHAPES[fam] for c, fam in w["calls"]}
+
+
+def roofline_time(M, N, K, peaks, fmt="int4", group=128, out="bf16"):
+    """The roofline bound of one call: max(algorithmic bytes / HBM, flops /
+    bf16 tensor peak), in seconds, and which of the two it is."""
+    from weight_only_bit_w4a16_gb300 import metrics
+    tb = metrics.call_bytes(fmt, M, N, K, group, out) / (peaks["hbm_gbs"] * 1e9)
+    tf = metrics.call_flops(M, N, K) / (peaks["bf16_tflops"] * 1e12)
+    return (tb, "hbm") if tb >= tf else (tf, "tensor")
+
+
+def sweep_inputs(w, shapes):
+    from weight_only_bit_w4a16_gb300 import synth
+    weights = {c: synth.make_weights(w["fmt"], N, K, w["group"], seed=500 + i)
+               for i, (c, (N, K)) in enumerate(shapes.items())}
+    Ks = sorted({K for _, K in shapes.values()})
+    A = {(M, K): synth.draw_A(np.random.default_rng(2000 + M + K), M, K) for M in w["Ms"] for K in Ks}
+    return weights, A
+
+
+def sweep_oracle_sample(w, shapes, weights, A, cols, peaks, seed=0):
+    """The oracle on `cols` output columns of every call of one step:
+    (seconds, roofline seconds of the sampled work)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    t = time.perf_counter()
+    bound = 0.0
+    for M in w["Ms"]:
+        for c, (N, K) in shapes.items():
+            n = min(cols, N)
+            pick = np.sort(rng.choice(N, size=n, replace=False))
+            pk, sc, zr = weights[c]
+            oracle.gemm(A[(M, K)], pk, sc, zr, w["fmt"], w["group"], cols=pick)
+            bound += roofline_time(M, N, K, peaks)[0] * n / N   # the sampled share of the call
+    return time.perf_counter() - t, bound
+
+
+def sweep_oracle_cols(w, shapes, weights, A, peaks, budget_s):
+    dt, _ = sweep_oracle_sample(w, shapes, weights, A, 1, peaks)
+    return int(max(1, min(64, budget_s / max(dt, 1e-6))))
+
+
+def run_sweep(args):
+    import torch
+    import weight_only_bit_w4a16_gb300 as wq
+
+    ws, rank = dist_init(use_cuda=True)
+    _, _, local = dist_env()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    wq.lib()   # fails loudly without the built library
+    w = BENCH_WORKLOADS[args.workload]
+    fmt, group, Ms = w["fmt"], w["group"], w["Ms"]
+    fcode = wq.FORMATS[fmt]
+    shapes = sweep_shapes(w)
+    peaks = measured_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 * 1024 * 1024)
+    prepacked = args.layout == "prepacked"
+    overlap = 0 if args.no_overlap else wq.WQ_LAUNCH_OVERLAP
+
+    weights_h, A_h = sweep_inputs(w, shapes)
+
+    def up(pk, sc, zr):
+        return (torch.from_numpy(pk).to(dev), torch.from_numpy(sc.view(np.int16)).to(dev),
+                torch.from_numpy(zr).to(dev))
+
+    def weight_set(c):
+        d = up(*weights_h[c])
+        return wq.prepack(*d, fmt, group) if prepacked else d
+
+    wsets = {c: weight_set(c) for c in shapes}
+    A_d = {key: torch.from_numpy(a.view(np.int16)).to(dev) for key, a in A_h.items()}
+    C_d = {(M, c): torch.empty((M, N), dtype=torch.bfloat16, device=dev) for M in Ms for c, (N, K) in shapes.items()}
+    # one workspace serves every call on the stream (completed calls leave its flags zero)
+    ws_bytes = max(wq.wq_gemm_workspace_size(M, N, K, fcode, group) for M in Ms for N, K in shapes.values())
+    work = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(dev)
+
+    def call(M, c, h, wset, flags=None, C=None):
+        N, K = shapes[c]
+        fl = wq.WQ_PATH_AUTO | (overlap if flags is None else flags)
+        A, Cd = A_d[(M, K)], (C if C is not None else C_d[(M, c)])
+        if prepacked:
+            st = wq.wq_gemm_prepacked(A.data_ptr(), wset.buf.data_ptr(), Cd.data_ptr(), M, N, K, fcode, group, None,
+                                      work.data_ptr(), ws_bytes, h, fl)
+        else:
+            pk, sc, zr = wset
+            st = wq.wq_gemm_ws(A.data_ptr(), pk.data_ptr(), sc.data_ptr(), zr.data_ptr(), Cd.data_ptr(), M, N, K,
+                               fcode, group, work.data_ptr(), ws_bytes, h, fl)
+        if st != wq.WQ_OK:
+            raise wq.WQError(st, f"{c} M={M}")
+
+    def one_step(h, flags=None):
+        for M in Ms:
+            for c in shapes:
+                call(M, c, h, wsets[c], flags)
+
+    def graph_of(fn, n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                h = torch.cuda.current_stream().cuda_stream
+                for i in range(n):
+                    fn(i, h)
+        return g
+
+    with torch.cuda.stream(s):
+        for _ in range(2):   # eager warm-up outside capture (module load, attributes)
+            one_step(s.cuda_stream)
+    torch.cuda.synchronize()
+    g_step = graph_of(lambda i, h: one_step(h), 1)
+    g_plain = graph_of(lambda i, h: one_step(h, 0), 1)
+    for _ in range(args.warmup):
+        g_step.replay()
+    torch.cuda.synchronize()
+
+    gpu_id = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else str(local)
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    with torch.cuda.stream(s):
+        ev0.record(s)
+        for _ in range(args.steps):
+            g_step.replay()
+        ev1.record(s)
+    torch.cuda.synchronize()
+    t1 = time.monotonic()
+    barrier()
+    time.sleep(0.15)
+    sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, dev)
+    clocks = sampler.summary(t0, t1)
+    step_s = ms_max / 1e3 / args.steps
+    bound_step = sum(roofline_time(M, N, K, peaks)[0] for M in Ms for N, K in shapes.values())
+    value = 100.0 * bound_step / step_s
+    flops_step = sum(2 * M * N * K for M in Ms for N, K in shapes.values())
+
+    with torch.cuda.stream(s):
+        g_plain.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(max(1, args.steps // 4)):
+            g_plain.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    plain_step_s = e0.elapsed_time(e1) / 1e3 / max(1, args.steps // 4)
+
+    # each (call shape, M) alone: back-to-back launches over weight copies
+    # rotated past L2, graph-timed; k/v and gate/up share a shape
+    per_shape = {}
+    for c, (N, K) in shapes.items():
+        fam = dict(w["calls"])[c]
+        if fam in per_shape:
+            continue
+        wb = sum(a.nbytes for a in weights_h[c])
+        R = max(2, math.ceil(2.0 * l2 / wb))
+        copies = [wsets[c]] + [weight_set(c) for _ in range(R - 1)]
+        n_calls = R * max(1, math.ceil(16 / R))
+        per_shape[fam] = {}
+        for M in Ms:
+            g = graph_of(lambda i, h, M=M: call(M, c, h, copies[i % R]), n_calls)
+            g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 3
+            with torch.cuda.stream(s):
+                e0.record(s)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(s)
+            torch.cuda.synchronize()
+            t_call = e0.elapsed_time(e1) / 1e3 / (reps * n_calls)
+            tb, bound = roofline_time(M, N, K, peaks)
+            per_shape[fam][str(M)] = {"N": N, "K": K, "us_per_call": t_call * 1e6,
+                                      "tflops": 2 * M * N * K / t_call / 1e12, "weight_GBps": wb / t_call / 1e9,
+                                      "bound": bound, "roofline_frac": tb / t_call}
+            del g
+        del copies
+    torch.cuda.synchronize()
+
+    # the dominant kernel of the step: the (shape, M) with the largest time share
+    share = {(fam, M): v["us_per_call"] * sum(1 for c2, f2 in w["calls"] if f2 == fam)
+             for fam, d in per_shape.items() for M, v in d.items()}
+    (dfam, dM), _ = max(share.items(), key=lambda kv: kv[1])
+    d = per_shape[dfam][dM]
+    M_d = int(dM)
+    if d["bound"] == "tensor":
+        algo = 2.0 * M_d * d["N"] * d["K"]
+        achieved = algo / (d["us_per_call"] * 1e-6) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": None, "algorithmic_flops_per_launch": algo,
+                "peak_source": peaks["source"] + " bf16_tflops (burst)"}
+    else:
+        from weight_only_bit_w4a16_gb300 import metrics
+        algo = metrics.call_bytes(fmt, M_d, d["N"], d["K"], group, "bf16")
+        achieved = algo / (d["us_per_call"] * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes_per_launch": algo,
+                "peak_source": peaks["source"] + " hbm_gbs"}
+    roof["kernel"] = f"{dfam} {d['N']}x{d['K']} at M={dM}, timed alone (back-to-back launches, weights rotated past L2)"
+    roof["step_share"] = share[(dfam, dM)] * 1e-6 / step_s
+
+    e2e = run_sweep_e2e(args, w, shapes, weights_h, A_h, wsets, prepacked, dev, ws, bound_step)
+
+    wbytes_step = sum(a.nbytes for c in shapes for a in weights_h[c])
+    result = {
+        "metric": w["metric"], "value": value, "unit": w["unit"], "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "format": fmt, "group": group, "M": list(Ms),
+                   "calls": {c: list(shapes[c]) for c in shapes}, "out": "bf16",
+                   "calls_per_step": len(Ms) * len(shapes),
+                   "l2": f"inputs larger than L2: a step streams {wbytes_step / 1e6:.0f} MB of weights per M "
+                         f"(L2 {l2 / 1e6:.0f} MB); a weight is reused only after all the others",
+                   "timing": "CUDA graph of one step, replayed; CUDA events on the launching stream",
+                   "launch": "WQ_LAUNCH_OVERLAP (programmatic dependent launch)" if overlap else "plain",
+                   "layout": ("prepacked (wq_prepack, untimed build step)" if prepacked else
+                              "as given (packed, scales, zeros)"),
+                   "workspace": f"{ws_bytes} B, shared by the calls (stream-K where the tiles fill the SMs badly)",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": roof, "clocks": clocks, "gpu_launches": args.steps * len(Ms) * len(shapes), "e2e": e2e,
+        "step": {"roofline_us": bound_step * 1e6, "measured_us": step_s * 1e6,
+                 "tflops": flops_step / step_s / 1e12},
+        "plain_launch": {"ms_per_step": plain_step_s * 1e3, "value": 100.0 * bound_step / plain_step_s},
+        "per_shape": per_shape,
+    }
+    if rank == 0 and ws == 1:
+        cols = sweep_oracle_cols(w, shapes, weights_h, A_h, peaks, args.cpu_budget)
+        dt, bound = sweep_oracle_sample(w, shapes, weights_h, A_h, cols, peaks, seed=1)
+        import oracle
+        result["cpu_baseline"] = {"value": 100.0 * bound / dt, "unit": w["unit"], "cores": oracle.max_threads(),
+                                  "kind": "oracle",
+                                  "sample": f"{cols} output columns of each of the step's {len(Ms) * len(shapes)} "
+                                            f"calls, {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def run_sweep_e2e(args, w, shapes, weights_h, A_h, wsets, prepacked, dev, ws, bound_step):
+    """The sweep through the public API (gemm_prepacked, or gemm with
+    --layout plain) from pinned host memory: per step one H2D copy of all the
+    step's activations and one D2H copy of all its results; the weights stay
+    device-resident (uploaded, and repacked, once)."""
+    import torch
+    import weight_only_bit_w4a16_gb300 as wq
+    Ms = w["Ms"]
+    keys = sorted(A_h)
+    a_elems = sum(A_h[k].size for k in keys)
+    A_h_all = torch.empty(a_elems, dtype=torch.bfloat16).pin_memory()
+    A_d_all = torch.empty(a_elems, dtype=torch.bfloat16, device=dev)
+    A_d, o = {}, 0
+    for k in keys:
+        M, K = k
+        n = M * K
+        A_h_all[o:o + n].copy_(torch.from_numpy(A_h[k].view(np.int16).reshape(-1)).view(torch.bfloat16))
+        A_d[k] = A_d_all[o:o + n].view(M, K)
+        o += n
+    c_elems = sum(M * N for M in Ms for N, _ in shapes.values())
+    C_h_all = torch.empty(c_elems, dtype=torch.bfloat16).pin_memory()
+    C_d_all = torch.empty(c_elems, dtype=torch.bfloat16, device=dev)
+    C_d, o = {}, 0
+    for M in Ms:
+        for c, (N, K) in shapes.items():
+            C_d[(M, c)] = C_d_all[o:o + M * N].view(M, N)
+            o += M * N
+    dev_w = None if prepacked else {c: wsets[c] for c in shapes}
+    s = torch.cuda.Stream(dev)
+
+    def one():
+        A_d_all.copy_(A_h_all, non_blocking=True)
+        j = 0
+        for M in Ms:
+            for c, (N, K) in shapes.items():
+                ov = not args.no_overlap and j > 0
+                if prepacked:
+                    wq.gemm_prepacked(A_d[(M, K)], wsets[c], out=C_d[(M, c)], overlap=ov,
+                                      workspace=wq.workspace(M, N, K, "int4", device=dev))
+                else:
+                    pk, sc, zr = dev_w[c]
+                    wq.gemm(A_d[(M, K)], pk, sc.view(torch.bfloat16), zr, "int4", out=C_d[(M, c)], overlap=ov,
+                            workspace=wq.workspace(M, N, K, "int4", device=dev))
+                j += 1
+        C_h_all.copy_(C_d_all, non_blocking=True)
+
+    steps = max(1, min(args.steps, 100))
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            one()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(steps):
+            one()
+        e1.record(s)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    return {"value": 100.0 * bound_step / (ms / 1e3 / steps), "unit": w["unit"],
+            "h2d_bytes_per_step": a_elems * 2, "d2h_bytes_per_step": c_elems * 2, "steps": steps,
+            "weights": "device-resident (uploaded once, untimed, as model weights)" +
+                       (", prepacked once (untimed)" if prepacked else ""),
+            "api": "gemm_prepacked" if prepacked else "gemm"}
+
+
+def run_reference_sweep(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    w = BENCH_WORKLOADS[args.workload]
+    shapes = sweep_shapes(w)
+    peaks = measured_peaks()
+    weights_h, A_h = sweep_inputs(w, shapes)
+    total = args.steps + args.warmup
+    cols = sweep_oracle_cols(w, shapes, weights_h, A_h, peaks, max(0.01, 90.0 / max(total, 1)))
+    for i in range(args.warmup):
+        sweep_oracle_sample(w, shapes, weights_h, A_h, cols, peaks, seed=100 + i)
+    t = bound = 0.0
+    for i in range(args.steps):
+        dt, b = sweep_oracle_sample(w, shapes, weights_h, A_h, cols, peaks, seed=i)
+        t += dt
+        bound += b
+    value = 100.0 * bound / t
+    sample = f"{cols} output columns of each of the step's {len(w['Ms']) * len(shapes)} calls, each step"
+    res = {"impl": "reference", "metric": w["metric"], "value": value, "unit": w["unit"],
+           "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3 / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": args.workload, "format": w["fmt"], "group": w["group"], "M": list(w["Ms"]),
+                      "calls": {c: list(shapes[c]) for c in shapes}, "out": w["out"]},
+           "cpu_baseline": {"value": value, "unit": w["unit"], "cores": oracle.max_threads(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": w["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+           "gpu_launches": 0}
+    print(json.dumps(res), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default 20000; layer_sweep 300)")
+    ap.add_argument("--warmup", type=int, default=None, help="warm-up steps (default 200; layer_sweep 10)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS), default="decode_int4")
     ap.add_argument("--layout", choices=["prepacked", "plain"], default="prepacked",
@@ -674,12 +1039,16 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     args = ap.parse_args(argv)
+    d_steps, d_warm = DEFAULT_STEPS.get(args.workload, (20000, 200))
+    args.steps = d_steps if args.steps is None else args.steps
+    args.warmup = d_warm if args.warmup is None else args.warmup
     if args.steps < 1 or args.warmup < 0:
         ap.error("--steps >= 1 and --warmup >= 0")
+    sweep = args.workload == "layer_sweep"
     if args.impl == "reference":
-        run_reference(args)
+        (run_reference_sweep if sweep else run_reference)(args)
     else:
-        run_ours(args)
+        (run_sweep if sweep else run_ours)(args)
 
 
 if __name__ == "__main__":

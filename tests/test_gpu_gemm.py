@@ -47,13 +47,11 @@ def test_large_nvfp4():
 @pytest.mark.parametrize("layer", list(synth.LAYER_SHAPES))
 @pytest.mark.parametrize("M", [1, 16, 128, 2048])
 def test_layer_sweep(layer, M):
-    if layer == "lm_head" and M == 2048:
-        pytest.skip("covered at M=128; 2048 x 128256 output is 0.5 GB")
+    """Every decoder projection at every M, the LM head at M = 2048 (a 0.5 GB
+    output, checked on the sampled rows and columns copied from the device)
+    included."""
     p = synth.layer_problem(layer, M)
-    if M <= 16:
-        check_sampled(p, "bf16", k=8, what=f"{layer} M={M}")
-    else:
-        check_sampled(p, "bf16", k=8, what=f"{layer} M={M}")
+    check_sampled(p, "bf16", k=8, what=f"{layer} M={M}")
 
 
 # -- both kernels on the same shapes ------------------------------------------

@@ -42,8 +42,6 @@ def test_small_m_layers_split():
 @pytest.mark.parametrize("layer", ["q", "kv", "gate_up", "down", "lm_head"])
 @pytest.mark.parametrize("M", [128, 2048])
 def test_layer_shapes(layer, M):
-    if layer == "lm_head" and M == 2048:
-        pytest.skip("2048 x 128256 output is 0.5 GB")
     p = synth.layer_problem(layer, M)
     ws, _ = ws_for(p)
     check_sampled(p, "bf16", k=8, workspace=ws, what=f"{layer} M={M} stream-K")

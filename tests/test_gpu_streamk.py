@@ -47,11 +47,16 @@ def test_layer_shapes(layer, M):
     check_sampled(p, "bf16", k=8, workspace=ws, what=f"{layer} M={M} stream-K")
 
 
-# few tiles and long K: every tile is shared by many CTAs (tens of partials)
+# few tiles and long K: every tile is shared by several CTAs -- as many as
+# the library's CTA count gives (about tiles x sqrt(k-steps x 128 / bm)), or,
+# forced, one per SM (tens of partials per tile)
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4", "int4"])
 @pytest.mark.parametrize("M,N,K", [(17, 384, 4096), (128, 128, 8192), (130, 257, 1024), (300, 1000, 4160),
                                    (64, 200, 640)])
-def test_many_partials(fmt, M, N, K):
+@pytest.mark.parametrize("ctas", ["model", "all"])
+def test_many_partials(fmt, M, N, K, ctas, monkeypatch):
+    if ctas == "all":
+        monkeypatch.setenv("WQ_TC_SK_G", "100000")   # capped at min(units, SMs)
     group = 64 if (fmt == "int4" and K % 128) else None   # K must be a multiple of the group
     p = synth.make_problem(fmt, M, N, K, group=group, seed=M + N + K)
     ws, n = ws_for(p)
@@ -62,7 +67,7 @@ def test_workspace_left_zero_and_reused():
     """Consecutive calls of different shapes on one workspace: each finds the
     flags it needs at zero (a stale flag would hand a consumer an old
     partial), and the flag words are zero again afterwards."""
-    # a one-tile shape (grid of 128 CTAs) between shapes with full grids
+    # a one-tile shape (a grid of a few CTAs) between shapes with larger grids
     shapes = [("int4", 128, 384, 4096), ("mxfp4", 17, 128, 8192), ("nvfp4", 300, 1000, 1024)]
     size = max(wq.wq_gemm_workspace_size(M, N, K, wq.FORMATS[f], synth.GROUP[f]) for f, M, N, K in shapes)
     ws = torch.zeros(size, dtype=torch.uint8, device="cuda")

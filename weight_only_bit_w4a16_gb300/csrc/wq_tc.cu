@@ -33,6 +33,7 @@
 // records WQ_ERR_DEVICE_TIMEOUT in the device status word, the CTA unwinds
 // (outstanding TMA copies and MMAs are waited for, again with a bound) and
 // frees its tensor memory.
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -588,15 +589,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float f[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
-                for (int c2 = cfirst; c2 < cta; ++c2) {
+                // the contributors' partials in increasing CTA order, two at a
+                // time: their 16 loads are in flight together, the sums keep
+                // the order (a tile of M = 128 rows split over ~19 CTAs waited
+                // ~18 L2 round trips per chunk one partial at a time)
+                auto add4 = [&](const float4 (&t)[8]) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const float4 t = __ldcg(partial_ptr(a, c2, ch, j, row));
-                        f[4 * j] += t.x;
-                        f[4 * j + 1] += t.y;
-                        f[4 * j + 2] += t.z;
-                        f[4 * j + 3] += t.w;
+                        f[4 * j] += t[j].x;
+                        f[4 * j + 1] += t[j].y;
+                        f[4 * j + 2] += t[j].z;
+                        f[4 * j + 3] += t[j].w;
                     }
+                };
+                int c2 = cfirst;
+                for (; c2 + 1 < cta; c2 += 2) {
+                    float4 t0[8], t1[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        t0[j] = __ldcg(partial_ptr(a, c2, ch, j, row));
+                        t1[j] = __ldcg(partial_ptr(a, c2 + 1, ch, j, row));
+                    }
+                    add4(t0);
+                    add4(t1);
+                }
+                if (c2 < cta) {
+                    float4 t0[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) t0[j] = __ldcg(partial_ptr(a, c2, ch, j, row));
+                    add4(t0);
                 }
                 const int mb = m0 + ch * 32;
                 if constexpr (EPI) {
@@ -836,6 +857,22 @@ TcPlan plan_tc(int M, int N, int K, int sms, bool allow_streamk, int fmt) {
     p.units = tiles * p.nks;
     p.streamk = sk;
     p.G = (int)(sk ? (p.units < sms ? p.units : sms) : (tiles < sms ? tiles : sms));
+    if (sk) {
+        // Fewer CTAs than SMs when the tiles are few: a CTA's k-steps shrink
+        // as 1 / G, but the owner of a tile adds the partials (bm x 128 fp32
+        // each) of the G / tiles CTAs sharing it.  The sum of the two is least
+        // near tiles x sqrt(nks x 128 / bm) (same GPU, CTA counts 16..152:
+        // int4 128 x 1024 x 3072 flat from 32 to 80 CTAs at 16.3 us against
+        // 23.5 us on 152; 256 x 3072 x 3072 21.7 us on 96 against 28.9 us).
+        const int g_max = p.G;
+        const double g = (double)tiles * std::sqrt((double)p.nks * 128.0 / bm);
+        const long long gi = (long long)(g + 0.5);
+        if (gi >= tiles && gi < g_max) p.G = (int)gi;
+        if (const char* e = getenv("WQ_TC_SK_G")) {   // tests, tuning: the stream-K CTA count, clamped
+            const int v = atoi(e);
+            if (v >= 1) p.G = v < g_max ? v : g_max;
+        }
+    }
     // the flag words cover every CTA a launch on this device can have, so a
     // later call with more CTAs never reads an earlier call's partials as flags
     p.ws_bytes = sk ? kFlagBytes(sms) + (size_t)p.G * kBN * bm * sizeof(float) : 0;

@@ -542,14 +542,86 @@ def fused_gate_up(w, dev, l2):
                      f"epilogue; unfused: two calls + torch silu and mul)", "per_m": out}
 
 
+# ---------------------------------------------------------------------------
+# end-to-end timing: copies in, calls, copies out, pipelined over the steps
+# ---------------------------------------------------------------------------
+def e2e_pipeline_ms(dev, nsteps, h2d, compute, d2h, nbuf=2, group=16):
+    """Milliseconds for nsteps end-to-end steps, max over ranks.  Step i
+    copies its inputs in on a copy stream (h2d(i, b)), runs its calls on the
+    compute stream (compute(i, b)) and copies its results out on a second
+    copy stream (d2h(i, b)), with device buffers b = i mod nbuf: step i's
+    copies overlap the neighbouring steps' calls, as a serving loop
+    double-buffers them.  Events order each buffer's reuse (step i + nbuf
+    writes buffer b only after step i has read its inputs and its results
+    are on the host).  Groups of `group` steps are captured in one CUDA graph
+    (the three streams forked from and joined to the capturing one) and
+    replayed; each replay fills and drains the pipeline once.  Returns the
+    milliseconds, the steps timed and the buffer of a replay's last step."""
+    import torch
+    s_c, s_in, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    group = max(1, min(group, nsteps))
+
+    def body(n):
+        fork = torch.cuda.Event()
+        fork.record(s_c)
+        s_in.wait_event(fork)
+        s_out.wait_event(fork)
+        ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+        ev_c = [torch.cuda.Event() for _ in range(nbuf)]
+        ev_out = [torch.cuda.Event() for _ in range(nbuf)]
+        for i in range(n):
+            b = i % nbuf
+            if i >= nbuf:
+                s_in.wait_event(ev_c[b])      # step i - nbuf has read buffer b's inputs
+            with torch.cuda.stream(s_in):
+                h2d(i, b)
+            ev_in[b].record(s_in)
+            s_c.wait_event(ev_in[b])
+            if i >= nbuf:
+                s_c.wait_event(ev_out[b])     # ... and its results are on the host
+            with torch.cuda.stream(s_c):
+                compute(i, b)
+            ev_c[b].record(s_c)
+            s_out.wait_event(ev_c[b])
+            with torch.cuda.stream(s_out):
+                d2h(i, b)
+            ev_out[b].record(s_out)
+        for st in (s_in, s_out):
+            join = torch.cuda.Event()
+            join.record(st)
+            s_c.wait_event(join)
+
+    with torch.cuda.stream(s_c):
+        body(min(nsteps, 2 * nbuf))      # eager warm-up (module load, first-call work)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s_c):
+        body(group)
+    reps = max(1, nsteps // group)
+    with torch.cuda.stream(s_c):
+        g.replay()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s_c):
+        e0.record(s_c)
+        for _ in range(reps):
+            g.replay()
+        e1.record(s_c)
+    torch.cuda.synchronize()
+    return max_over_ranks(e0.elapsed_time(e1), dev), reps * group, (group - 1) % nbuf
+
+
 def run_e2e(args, w, A_by_M, weights, pool, dev, ws, pre_pool=None):
     """The same metric through the public API (weight_only_bit_w4a16_gb300.gemm,
     or gemm_prepacked on prepacked weights) from pinned host memory.  Per
     step: one H2D copy of the step's activations (all its calls' A, packed
     in one pinned buffer), the calls chained on device-resident weights
     (uploaded -- and repacked -- once, as a model's weights are), one D2H
-    copy of all the step's results.  A second figure also uploads the
-    weights every step (and repacks them, for the prepacked layout)."""
+    copy of all the step's results -- pipelined over the steps
+    (e2e_pipeline_ms).  "serial" reports the same steps issued one after
+    another on one stream, and "with_weight_upload" serial steps that also
+    upload (and repack) every weight."""
     import torch
     import weight_only_bit_w4a16_gb300 as wq
     from weight_only_bit_w4a16_gb300 import metrics
@@ -610,15 +682,62 @@ def run_e2e(args, w, A_by_M, weights, pool, dev, ws, pre_pool=None):
 
     h2d = A_h_all.numel() * 2
     d2h = C_h_all.numel() * C_h_all.element_size()
-    ms = timed(steps)
     wbytes = metrics.weight_bytes(fmt, N, K, group)
-    if w["unit"] == "GB/s":
-        val = ws * steps * wbytes * len(Ms) / (ms / 1e3) / 1e9
-    else:
-        val = ws * steps * sum(metrics.call_flops(M, N, K) for M in Ms) / (ms / 1e3) / 1e12
-    res = {"value": val, "unit": w["unit"], "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "steps": steps, "weights": "device-resident (uploaded once, untimed, as model weights)" +
-                                      (", prepacked once (untimed)" if pre_pool is not None else ""),
+
+    def rate(ms_, n_):
+        if w["unit"] == "GB/s":
+            return ws * n_ * wbytes * len(Ms) / (ms_ / 1e3) / 1e9
+        return ws * n_ * sum(metrics.call_flops(M, N, K) for M in Ms) / (ms_ / 1e3) / 1e12
+
+    # pipelined: double-buffered device inputs and outputs, one pinned host
+    # output buffer per device one
+    A_buf = [A_d_all, torch.empty_like(A_d_all)]
+    C_buf = [C_d_all, torch.empty_like(C_d_all)]
+    C_hb = [C_h_all, torch.empty(C_h_all.shape, dtype=odt).pin_memory()]
+    views = []
+    for b_ in range(2):
+        vA, vC, r0 = {}, {}, 0
+        for M in Ms:
+            vA[M], vC[M] = A_buf[b_][r0:r0 + M], C_buf[b_][r0:r0 + M]
+            r0 += M
+        views.append((vA, vC))
+
+    def p_h2d(i, b_):
+        A_buf[b_].copy_(A_h_all, non_blocking=True)
+
+    def p_compute(i, b_):
+        vA, vC = views[b_]
+        for j, M in enumerate(Ms):
+            slot = (i * len(Ms) + j) % R
+            if pre_pool is not None:
+                wq.gemm_prepacked(vA[M], pre_pool[slot], out_dtype=out, out=vC[M], overlap=overlap and j > 0)
+            else:
+                pk, sc, zr = pool[slot]
+                wq.gemm(vA[M], pk, sc, zr, fmt, group, out_dtype=out, out=vC[M], overlap=overlap and j > 0)
+
+    def p_d2h(i, b_):
+        C_hb[b_].copy_(C_buf[b_], non_blocking=True)
+
+    group_steps = R // math.gcd(R, len(Ms)) if R % len(Ms) else R // len(Ms)   # whole weight rotations
+    group_steps *= max(1, 16 // group_steps)
+    ms_p, n_p, last = e2e_pipeline_ms(dev, steps, p_h2d, p_compute, p_d2h, group=group_steps)
+    # the pipeline's last results on the host against the same step run alone
+    # (every weight set holds the same weights; the kernels are deterministic)
+    with torch.cuda.stream(s):
+        A_buf[1 - last].copy_(A_h_all)
+        p_compute(0, 1 - last)
+    torch.cuda.synchronize()
+    checked = bool(torch.equal(C_hb[last].view(torch.int16 if out != "fp32" else torch.int32),
+                               C_buf[1 - last].cpu().view(torch.int16 if out != "fp32" else torch.int32)))
+    ms = timed(steps)
+    res = {"value": rate(ms_p, n_p), "unit": w["unit"], "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": n_p, "pipeline": "copy-in / calls / copy-out streams, double-buffered, "
+                                     f"{group_steps} steps per CUDA graph",
+           "results_checked": checked,
+           "serial": {"value": rate(ms, steps), "steps": steps,
+                      "how": "each step's copies and calls in order on one stream, Python-issued"},
+           "weights": "device-resident (uploaded once, untimed, as model weights)" +
+                      (", prepacked once (untimed)" if pre_pool is not None else ""),
            "api": "gemm_prepacked" if pre_pool is not None else "gemm"}
     # every step also uploads its weights from pinned host memory
     pk_h = torch.from_numpy(weights[0]).pin_memory()
@@ -626,11 +745,7 @@ def run_e2e(args, w, A_by_M, weights, pool, dev, ws, pre_pool=None):
     zr_h = None if weights[2] is None else torch.from_numpy(weights[2]).pin_memory()
     steps_w = max(1, min(args.steps, 100))
     ms_w = timed(steps_w, (pk_h, sc_h, zr_h))
-    if w["unit"] == "GB/s":
-        val_w = ws * steps_w * wbytes * len(Ms) / (ms_w / 1e3) / 1e9
-    else:
-        val_w = ws * steps_w * sum(metrics.call_flops(M, N, K) for M in Ms) / (ms_w / 1e3) / 1e12
-    res["with_weight_upload"] = {"value": val_w, "unit": w["unit"],
+    res["with_weight_upload"] = {"value": rate(ms_w, steps_w), "unit": w["unit"],
                                  "h2d_bytes_per_step": h2d + wbytes * len(Ms), "d2h_bytes_per_step": d2h,
                                  "steps": steps_w}
     return res
@@ -929,65 +1044,74 @@ def run_sweep(args):
 def run_sweep_e2e(args, w, shapes, weights_h, A_h, wsets, prepacked, dev, ws, bound_step):
     """The sweep through the public API (gemm_prepacked, or gemm with
     --layout plain) from pinned host memory: per step one H2D copy of all the
-    step's activations and one D2H copy of all its results; the weights stay
-    device-resident (uploaded, and repacked, once)."""
+    step's activations and one D2H copy of all its results, pipelined over
+    the steps (e2e_pipeline_ms); the weights stay device-resident (uploaded,
+    and repacked, once)."""
     import torch
     import weight_only_bit_w4a16_gb300 as wq
     Ms = w["Ms"]
     keys = sorted(A_h)
     a_elems = sum(A_h[k].size for k in keys)
-    A_h_all = torch.empty(a_elems, dtype=torch.bfloat16).pin_memory()
-    A_d_all = torch.empty(a_elems, dtype=torch.bfloat16, device=dev)
-    A_d, o = {}, 0
-    for k in keys:
-        M, K = k
-        n = M * K
-        A_h_all[o:o + n].copy_(torch.from_numpy(A_h[k].view(np.int16).reshape(-1)).view(torch.bfloat16))
-        A_d[k] = A_d_all[o:o + n].view(M, K)
-        o += n
     c_elems = sum(M * N for M in Ms for N, _ in shapes.values())
-    C_h_all = torch.empty(c_elems, dtype=torch.bfloat16).pin_memory()
-    C_d_all = torch.empty(c_elems, dtype=torch.bfloat16, device=dev)
-    C_d, o = {}, 0
-    for M in Ms:
-        for c, (N, K) in shapes.items():
-            C_d[(M, c)] = C_d_all[o:o + M * N].view(M, N)
-            o += M * N
-    dev_w = None if prepacked else {c: wsets[c] for c in shapes}
-    s = torch.cuda.Stream(dev)
+    A_h_all = torch.empty(a_elems, dtype=torch.bfloat16).pin_memory()
+    o = 0
+    for k in keys:
+        n = A_h[k].size
+        A_h_all[o:o + n].copy_(torch.from_numpy(A_h[k].view(np.int16).reshape(-1)).view(torch.bfloat16))
+        o += n
+    nbuf = 2
+    A_buf = [torch.empty(a_elems, dtype=torch.bfloat16, device=dev) for _ in range(nbuf)]
+    C_buf = [torch.empty(c_elems, dtype=torch.bfloat16, device=dev) for _ in range(nbuf)]
+    C_hb = [torch.empty(c_elems, dtype=torch.bfloat16).pin_memory() for _ in range(nbuf)]
+    views = []
+    for b in range(nbuf):
+        vA, vC, o = {}, {}, 0
+        for k in keys:
+            M, K = k
+            vA[k] = A_buf[b][o:o + M * K].view(M, K)
+            o += M * K
+        o = 0
+        for M in Ms:
+            for c, (N, K) in shapes.items():
+                vC[(M, c)] = C_buf[b][o:o + M * N].view(M, N)
+                o += M * N
+        views.append((vA, vC))
+    work = {(M, c): wq.workspace(M, N, K, "int4", device=dev) for M in Ms for c, (N, K) in shapes.items()}
+    # wq.workspace grows one cached buffer: take the largest once, for every call
+    big = max((t for t in work.values() if t is not None), key=lambda t: t.numel(), default=None)
 
-    def one():
-        A_d_all.copy_(A_h_all, non_blocking=True)
+    def h2d(i, b):
+        A_buf[b].copy_(A_h_all, non_blocking=True)
+
+    def compute(i, b):
+        vA, vC = views[b]
         j = 0
         for M in Ms:
             for c, (N, K) in shapes.items():
                 ov = not args.no_overlap and j > 0
+                wsp = big if work[(M, c)] is not None else None
                 if prepacked:
-                    wq.gemm_prepacked(A_d[(M, K)], wsets[c], out=C_d[(M, c)], overlap=ov,
-                                      workspace=wq.workspace(M, N, K, "int4", device=dev))
+                    wq.gemm_prepacked(vA[(M, K)], wsets[c], out=vC[(M, c)], overlap=ov, workspace=wsp)
                 else:
-                    pk, sc, zr = dev_w[c]
-                    wq.gemm(A_d[(M, K)], pk, sc.view(torch.bfloat16), zr, "int4", out=C_d[(M, c)], overlap=ov,
-                            workspace=wq.workspace(M, N, K, "int4", device=dev))
+                    pk, sc, zr = wsets[c]
+                    wq.gemm(vA[(M, K)], pk, sc, zr, "int4", out=vC[(M, c)], overlap=ov, workspace=wsp)
                 j += 1
-        C_h_all.copy_(C_d_all, non_blocking=True)
 
-    steps = max(1, min(args.steps, 100))
+    def d2h(i, b):
+        C_hb[b].copy_(C_buf[b], non_blocking=True)
+
+    steps = max(1, min(args.steps, 96))
+    ms, n, last = e2e_pipeline_ms(dev, steps, h2d, compute, d2h, nbuf=nbuf, group=8)
+    # the pipeline's last results on the host against the same step run alone
+    s = torch.cuda.Stream(dev)
     with torch.cuda.stream(s):
-        for _ in range(3):
-            one()
+        A_buf[1 - last].copy_(A_h_all)
+        compute(0, 1 - last)
     torch.cuda.synchronize()
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(s):
-        e0.record(s)
-        for _ in range(steps):
-            one()
-        e1.record(s)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(e0.elapsed_time(e1), dev)
-    return {"value": 100.0 * bound_step / (ms / 1e3 / steps), "unit": w["unit"],
-            "h2d_bytes_per_step": a_elems * 2, "d2h_bytes_per_step": c_elems * 2, "steps": steps,
+    checked = bool(torch.equal(C_hb[last].view(torch.int16), C_buf[1 - last].cpu().view(torch.int16)))
+    return {"value": 100.0 * bound_step / (ms / 1e3 / n), "unit": w["unit"], "results_checked": checked,
+            "h2d_bytes_per_step": a_elems * 2, "d2h_bytes_per_step": c_elems * 2, "steps": n,
+            "pipeline": "copy-in / calls / copy-out streams, double-buffered, 8 steps per CUDA graph",
             "weights": "device-resident (uploaded once, untimed, as model weights)" +
                        (", prepacked once (untimed)" if prepacked else ""),
             "api": "gemm_prepacked" if prepacked else "gemm"}

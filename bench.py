@@ -246,16 +246,47 @@ def host_inputs(w, seed=0):
     return A_by_M, weights
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), else the machine type."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
+
+
+def one_core(measure, budget_s):
+    """measure(budget) -> dict on one oracle thread; the thread count is restored."""
+    import oracle
+    n = oracle.max_threads()
+    oracle.set_threads(1)
+    try:
+        return measure(budget_s)
+    finally:
+        oracle.set_threads(n)
+
+
 def cpu_baseline(w, A_by_M, weights, budget_s=15.0):
     import oracle
-    cols = oracle_rate(w, A_by_M, weights, budget_s)
-    dt, covered = oracle_step_sample(w, cols, A_by_M, weights, seed=1)
     from weight_only_bit_w4a16_gb300 import metrics
-    flops = sum(metrics.call_flops(M, cols, w["K"]) for M in w["Ms"])
-    value = covered / dt / 1e9 if w["unit"] == "GB/s" else flops / dt / 1e12
-    return {"value": value, "unit": w["unit"], "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"{cols} of {w['N']} output columns of each call of one step "
-                      f"(M={list(w['Ms'])}, K={w['K']}), {dt:.1f} s"}
+
+    def measure(budget):
+        cols = oracle_rate(w, A_by_M, weights, budget)
+        dt, covered = oracle_step_sample(w, cols, A_by_M, weights, seed=1)
+        flops = sum(metrics.call_flops(M, cols, w["K"]) for M in w["Ms"])
+        value = covered / dt / 1e9 if w["unit"] == "GB/s" else flops / dt / 1e12
+        return {"value": value, "sample": f"{cols} of {w['N']} output columns of each call of one step "
+                                          f"(M={list(w['Ms'])}, K={w['K']}), {dt:.1f} s"}
+
+    res = measure(budget_s)
+    single = one_core(measure, max(0.05, budget_s / 4))
+    return {"value": res["value"], "unit": w["unit"], "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": res["sample"], "cpu": cpu_model(),
+            "one_core": {"value": single["value"], "unit": w["unit"], "sample": single["sample"]}}
 
 
 # ---------------------------------------------------------------------------
@@ -785,7 +816,7 @@ def run_reference(args):
            "config": {"workload": args.workload, "format": w["fmt"], "group": w["group"], "M": list(w["Ms"]),
                       "N": w["N"], "K": w["K"], "out": w["out"]},
            "cpu_baseline": {"value": value, "unit": w["unit"], "cores": oracle.max_threads(),
-                            "kind": "oracle", "sample": sample},
+                            "kind": "oracle", "sample": sample, "cpu": cpu_model()},
            "e2e": {"value": value, "unit": w["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
            "gpu_launches": 0}
     print(json.dumps(res), flush=True)
@@ -1030,13 +1061,20 @@ def run_sweep(args):
         "per_shape": per_shape,
     }
     if rank == 0 and ws == 1:
-        cols = sweep_oracle_cols(w, shapes, weights_h, A_h, peaks, args.cpu_budget)
-        dt, bound = sweep_oracle_sample(w, shapes, weights_h, A_h, cols, peaks, seed=1)
         import oracle
-        result["cpu_baseline"] = {"value": 100.0 * bound / dt, "unit": w["unit"], "cores": oracle.max_threads(),
-                                  "kind": "oracle",
-                                  "sample": f"{cols} output columns of each of the step's {len(Ms) * len(shapes)} "
-                                            f"calls, {dt:.1f} s"}
+
+        def measure(budget):
+            cols = sweep_oracle_cols(w, shapes, weights_h, A_h, peaks, budget)
+            dt, bound = sweep_oracle_sample(w, shapes, weights_h, A_h, cols, peaks, seed=1)
+            return {"value": 100.0 * bound / dt,
+                    "sample": f"{cols} output columns of each of the step's {len(Ms) * len(shapes)} calls, {dt:.1f} s"}
+
+        res = measure(args.cpu_budget)
+        single = one_core(measure, max(0.05, args.cpu_budget / 4))
+        result["cpu_baseline"] = {"value": res["value"], "unit": w["unit"], "cores": oracle.max_threads(),
+                                  "kind": "oracle", "sample": res["sample"], "cpu": cpu_model(),
+                                  "one_core": {"value": single["value"], "unit": w["unit"],
+                                               "sample": single["sample"]}}
     if rank == 0:
         print(json.dumps(result), flush=True)
 
@@ -1143,7 +1181,7 @@ def run_reference_sweep(args):
            "config": {"workload": args.workload, "format": w["fmt"], "group": w["group"], "M": list(w["Ms"]),
                       "calls": {c: list(shapes[c]) for c in shapes}, "out": w["out"]},
            "cpu_baseline": {"value": value, "unit": w["unit"], "cores": oracle.max_threads(),
-                            "kind": "oracle", "sample": sample},
+                            "kind": "oracle", "sample": sample, "cpu": cpu_model()},
            "e2e": {"value": value, "unit": w["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
            "gpu_launches": 0}
     print(json.dumps(res), flush=True)

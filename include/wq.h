@@ -74,7 +74,9 @@ extern "C" {
  * GEMV kernel starts streaming its weights while the preceding kernel on the
  * stream is still running (A is read and C written only after that kernel
  * has completed).  The caller guarantees that the preceding kernel does not
- * write packed, scales or zeros -- true whenever they are model weights. */
+ * write packed, scales, zeros or the prepacked buffer -- true whenever they
+ * are model weights, and false right after the wq_prepack that writes them
+ * (synchronise first). */
 #define WQ_LAUNCH_OVERLAP 0x100
 
 /* status codes */

@@ -110,7 +110,7 @@ int wq_gemm_ex(const void* A, const uint8_t* packed, const void* scales, const u
  * tile whose k-steps are shared by two or more CTAs is finished by the CTA
  * holding its last k-step, which adds the fp32 partial sums the others left
  * in the workspace, in a fixed CTA order -- deterministic, no atomics on C).
- * The paper pages have no counterpart; it is a load-balancing device of this
+ * The method itself has no such step: it is a load-balancing device of this
  * library and computes the same sum of products as wq_gemm_ex.
  *   workspace        256-byte aligned device memory (NULL with 0 bytes: the
  *                    call behaves as wq_gemm_ex).  It must hold zeros before
@@ -134,7 +134,7 @@ int wq_gemm_ws(const void* A, const uint8_t* packed, const void* scales, const u
  * wq_gemm_static -- wq_gemm_ws with the library's own scratch instead of a
  * caller-owned workspace: a fixed device array inside the library (room for
  * the split tiles of up to 160 SMs), found once per device, so the call
- * allocates nothing.  The paper pages have no counterpart; it exists so that
+ * allocates nothing.  The method itself has no such step; it exists so that
  * a caller without a memory allocator still gets the balanced tensor-core
  * path.  Limits: one scratch per device, so calls through this entry point
  * must be ordered on the device (one stream at a time), and a shape whose

@@ -41,7 +41,7 @@
  *   - NVFP4 applies |e4m3(scale)| ([P3] wording); the sign bit is ignored.
  *   - e4m3fn: bias 7, exponent 0 subnormal, S.1111.111 is NaN, no infinity.
  *   - e8m0 0x00 is 2^-127 (not zero); 0xFF is NaN.
- *   - int4 zero is read as a full uint8 (the pages promise 0..15).
+ *   - int4 zero is read as a full uint8 (the KBench spec's weight format gives 0..15).
  *   - No second-level per-tensor NVFP4 scale.
  */
 #include <math.h>

@@ -100,6 +100,8 @@ struct TcArgs {
     long long units;    // tiles * nks
     int G;              // CTAs of a stream-K launch
     int kblocks;        // prepacked weights: 128-k blocks per row
+    int vec_store;      // C rows 16-byte aligned and the store scratch allocated: vector stores of C
+    int scr_off;        // byte offset of the decode warps' store scratch (2 KB each) in shared memory
     Epilogue epi;
 };
 
@@ -628,6 +630,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float u = a.epi.gated ? __shfl_xor_sync(0xffffffffu, f[j], 8) : 0.f;
                         if (mine && mb + j < a.M) store_epilogue(a.epi, a.C, a.out_f32, a.N, mb + j, n, f[j], u);
                     }
+                } else if (a.vec_store) {
+                    // This warp's 32 weight rows x 32 activation rows through its
+                    // 2 KB of shared memory, transposed, then out as 16-byte
+                    // pieces of C rows: 4 vector stores per lane where 32 scalar
+                    // ones wrote 64-byte pieces.
+                    const int nb = n - lane;                        // the warp's first weight row
+                    uint8_t* scr = smem + a.scr_off + (warp - 2) * 2048;
+                    if (a.out_f32) {
+                        float* t = reinterpret_cast<float*>(scr);   // [16 activation rows][32]
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) t[j * 32 + lane] = f[16 * h + j];
+                            __syncwarp();
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) {
+                                const int v = r * 32 + lane, row = v >> 3, c = (v & 7) * 4;
+                                const int m = mb + 16 * h + row;
+                                const float4 x = *reinterpret_cast<const float4*>(t + row * 32 + c);
+                                if (m < a.M && nb + c < a.N)
+                                    *reinterpret_cast<float4*>(static_cast<float*>(a.C) + (size_t)m * a.N + nb + c) = x;
+                            }
+                            __syncwarp();
+                        }
+                    } else {
+                        __nv_bfloat16* t = reinterpret_cast<__nv_bfloat16*>(scr);   // [32 activation rows][32]
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) t[j * 32 + lane] = __float2bfloat16_rn(f[j]);
+                        __syncwarp();
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const int v = r * 32 + lane, row = v >> 2, c = (v & 3) * 8;
+                            const int m = mb + row;
+                            const uint4 x = *reinterpret_cast<const uint4*>(t + row * 32 + c);
+                            if (m < a.M && nb + c < a.N)
+                                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.C) + (size_t)m * a.N + nb + c) = x;
+                        }
+                        __syncwarp();
+                    }
                 } else if (n < a.N) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
@@ -955,7 +996,19 @@ int run_tc(const void* A, const CUtensorMap& tp, bool pre, const uint8_t* scales
         fprintf(stderr, "wq: tcgen05%s M=%d N=%d K=%d: bm=%d tiles=%d %s grid=%d\n", pre ? " (prepacked)" : "", M, N,
                 K, bm, plan.tiles, plan.streamk ? "stream-K" : "data-parallel", plan.G);
     const dim3 grid(plan.G, 1, 1);
-    const size_t smem = 1024 + (size_t)kStages * args.stage_bytes + sizeof(TcShared);
+    size_t smem = 1024 + (size_t)kStages * args.stage_bytes + sizeof(TcShared);
+    // Stream-K launches stage C through the decode warps' store scratch (2 KB
+    // each) and write it in 16-byte pieces, where the output rows are 16-byte
+    // aligned: there the owner's stores are on the critical path (same GPU:
+    // int4 128 x 3072 x 3072 17.7 -> 16.8 us, 128 x 3072 x 8192 24.1 -> 23.3
+    // us).  Whole-tile launches keep the scalar stores, which overlap other
+    // tiles' work (with the scratch: 8192^3 NVFP4 778 -> 782 us).
+    constexpr size_t kScrBytes = (size_t)kDecodeSets * 4 * 2048;
+    constexpr size_t kMaxDynSmem = 227 * 1024;
+    args.scr_off = (int)(((size_t)kStages * args.stage_bytes + sizeof(TcShared) + 255) / 256 * 256);
+    args.vec_store = plan.streamk && (N % (out_f32 ? 4 : 8) == 0) &&
+                     1024 + (size_t)args.scr_off + kScrBytes <= kMaxDynSmem;
+    if (args.vec_store) smem = 1024 + (size_t)args.scr_off + kScrBytes;
     switch (fmt) {
         case kNVFP4:
             return pre ? launch_fmt<kNVFP4, true>(ta, tp, args, grid, smem, stream)

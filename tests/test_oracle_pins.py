@@ -66,7 +66,9 @@ def ind_dequant(packed, scales, zeros, fmt, group):
         return ind_e2m1(codes) * np.abs(ind_e4m3(scales))[:, g]
     if fmt == "mxfp4":
         return ind_e2m1(codes) * ind_e8m0(scales)[:, g]
-    return (codes - zeros.astype(np.int64)[:, g]) * ind_bf16(scales)[:, g]
+    # An infinite scale times a zero offset is NaN, the same as the oracle's IEEE product.
+    with np.errstate(invalid="ignore"):
+        return (codes - zeros.astype(np.int64)[:, g]) * ind_bf16(scales)[:, g]
 
 
 def bf16_of_exact(x):

@@ -78,6 +78,17 @@ extern "C" {
  * are model weights, and false right after the wq_prepack that writes them
  * (synchronise first). */
 #define WQ_LAUNCH_OVERLAP 0x100
+/* OR into `path` (small-M kernels; implies WQ_LAUNCH_OVERLAP): the caller
+ * declares that A, like the weights, is written by no kernel that can still
+ * be running -- i.e. it was complete before the most recent operation on the
+ * stream launched WITHOUT WQ_LAUNCH_OVERLAP / WQ_LAUNCH_INPUTS_READY began.
+ * The kernel then reads A and runs its whole product at once, and waits for
+ * the preceding kernel only before it stores C, so a chain of such calls
+ * (projections that share one input, independent weights of one step)
+ * overlaps end to end while still completing in stream order: a later
+ * operation on the stream sees the results of every earlier call.  The
+ * tensor-core path ignores the bit. */
+#define WQ_LAUNCH_INPUTS_READY 0x200
 
 /* status codes */
 #define WQ_OK 0

@@ -25,6 +25,7 @@ WQ_NVFP4, WQ_MXFP4, WQ_INT4 = 0, 1, 2
 WQ_OUT_F32 = 0x100
 WQ_PATH_AUTO, WQ_PATH_GEMV, WQ_PATH_TC = 0, 1, 2
 WQ_LAUNCH_OVERLAP = 0x100
+WQ_LAUNCH_INPUTS_READY = 0x200
 WQ_OK = 0
 WQ_ERR_INVALID_ARG = -1
 WQ_ERR_UNSUPPORTED = -2

@@ -163,8 +163,9 @@ WQ_EXPORT int wq_gemm_prepacked(const void* A, const void* prepacked, void* C, i
     if (format & ~(0xFF | WQ_OUT_F32)) return WQ_ERR_INVALID_ARG;
     const int fmt = format & 0xFF;
     if (M < 0 || N < 0 || K < 0) return WQ_ERR_INVALID_ARG;
-    if (path & ~(0xFF | WQ_LAUNCH_OVERLAP)) return WQ_ERR_INVALID_ARG;
-    const bool overlap = (path & WQ_LAUNCH_OVERLAP) != 0;
+    if (path & ~(0xFF | WQ_LAUNCH_OVERLAP | WQ_LAUNCH_INPUTS_READY)) return WQ_ERR_INVALID_ARG;
+    const bool inputs_ready = (path & WQ_LAUNCH_INPUTS_READY) != 0;
+    const bool overlap = (path & WQ_LAUNCH_OVERLAP) != 0 || inputs_ready;
     const int route = path & 0xFF;
     if (route != WQ_PATH_AUTO && route != WQ_PATH_GEMV && route != WQ_PATH_TC) return WQ_ERR_INVALID_ARG;
     if (workspace_bytes > 0 && !workspace) return WQ_ERR_INVALID_ARG;
@@ -195,7 +196,7 @@ WQ_EXPORT int wq_gemm_prepacked(const void* A, const void* prepacked, void* C, i
                                                workspace_bytes, epi, s);
         if (st != WQ_ERR_UNSUPPORTED) return st;
     }
-    return wq::launch_gemv_prepacked(A, prepacked, C, M, N, K, fmt, out_f32, overlap, epi, s);
+    return wq::launch_gemv_prepacked(A, prepacked, C, M, N, K, fmt, out_f32, overlap, inputs_ready, epi, s);
 }
 
 WQ_EXPORT int wq_dequant(const uint8_t* packed, const void* scales, const uint8_t* zeros, void* W, int N, int K,

@@ -69,6 +69,7 @@ struct PreArgs {
     int rb, wk_log2, ipw;
     uint32_t SA;            // shared row stride of the activations (bytes)
     uint32_t w_off, a_off, r_off, red_off;
+    int inputs_ready;       // A may be read before the preceding kernel completes
     Epilogue epi;
 };
 
@@ -257,10 +258,11 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_pre_kernel(const Pr
         two = __any_sync(0xffffffffu, two);
     }
 
-    // the next kernel on the stream may start; A is read, and C written, only
-    // after the preceding kernel has finished
+    // the next kernel on the stream may start.  C is written only after the
+    // preceding kernel has finished; A is read after it too, unless the
+    // caller declared it complete already (inputs_ready)
     grid_dependents_launch();
-    grid_dependency_wait();
+    if (!a.inputs_ready) grid_dependency_wait();
 
     // ---- 3. activations of this K range: the range's first warp copies them
     if (blk == 0) {
@@ -316,6 +318,7 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_pre_kernel(const Pr
         }
     }
     if (!ok && lane == 0) record_pre_timeout();
+    if (a.inputs_ready) grid_dependency_wait();   // completion order: stores after the predecessor's
     if (__syncthreads_or(!ok)) return;   // a copy never landed: store nothing
 
     // ---- 5. partial sums -> shared memory, fixed-order reduction, store ----
@@ -474,7 +477,8 @@ struct PlanKey {
 }  // namespace
 
 int launch_gemv_prepacked(const void* A, const void* prepacked, void* C, int M, int N, int K, int fmt,
-                          bool out_f32, bool pdl, const Epilogue& epi, cudaStream_t stream) {
+                          bool out_f32, bool pdl, bool inputs_ready, const Epilogue& epi, cudaStream_t stream) {
+    if (inputs_ready) pdl = true;
     if (M == 0 || N == 0) return WQ_OK;
     if (K <= 0 || K > kMaxIpw * (1 << kMaxWkLog2) * 128) return WQ_ERR_UNSUPPORTED;
     const int I = (K + 127) / 128, Nb = (N + 15) / 16;
@@ -550,6 +554,7 @@ int launch_gemv_prepacked(const void* A, const void* prepacked, void* C, int M, 
     args.a_off = plan.a_off;
     args.r_off = plan.r_off;
     args.red_off = plan.red_off;
+    args.inputs_ready = inputs_ready ? 1 : 0;
     args.epi = epi;
 
     cudaLaunchConfig_t cfg = {};

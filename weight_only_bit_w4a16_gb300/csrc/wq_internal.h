@@ -49,8 +49,11 @@ int launch_tc_prepacked(const void* A, const void* prepacked, void* C, int M, in
 size_t prepack_bytes(int N, int K, int fmt);
 int launch_prepack(const uint8_t* packed, const void* scales, const uint8_t* zeros, void* out, int N, int K,
                    int fmt, cudaStream_t stream);
+// inputs_ready: A was complete before the chain of overlapped launches began,
+// so the kernel reads it at once and waits for its predecessor only before
+// storing C (implies pdl)
 int launch_gemv_prepacked(const void* A, const void* prepacked, void* C, int M, int N, int K, int fmt,
-                          bool out_f32, bool pdl, const Epilogue& epi, cudaStream_t stream);
+                          bool out_f32, bool pdl, bool inputs_ready, const Epilogue& epi, cudaStream_t stream);
 
 // The library's own stream-K scratch (a file-scope device array of the
 // tensor-core module) on the current device and its size; NULL if the

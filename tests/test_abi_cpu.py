@@ -80,7 +80,7 @@ def test_gemm_argument_validation(args, expect):
 
 def test_gemm_bad_path():
     assert wq.wq_gemm_ex(FAKE, FAKE, FAKE, None, FAKE, 4, 8, 64, 0, 16, None, 9) == wq.WQ_ERR_INVALID_ARG
-    assert wq.wq_gemm_ex(FAKE, FAKE, FAKE, None, FAKE, 4, 8, 64, 0, 16, None, 0x200) == wq.WQ_ERR_INVALID_ARG
+    assert wq.wq_gemm_ex(FAKE, FAKE, FAKE, None, FAKE, 4, 8, 64, 0, 16, None, 0x400) == wq.WQ_ERR_INVALID_ARG
     # the overlap flag is a valid path bit (M == 0: validated, nothing launched)
     assert wq.wq_gemm_ex(FAKE, FAKE, FAKE, None, FAKE, 0, 8, 64, 0, 16, None,
                          wq.WQ_PATH_GEMV | wq.WQ_LAUNCH_OVERLAP) == wq.WQ_OK
@@ -152,7 +152,7 @@ def test_gemm_prepacked_argument_checks():
     assert f(FAKE, FAKE, FAKE, 0, 32, 256, 0, 16) == wq.WQ_OK                        # M == 0: no-op
     assert f(FAKE, FAKE, FAKE, 4, 0, 256, 0, 16) == wq.WQ_OK                         # N == 0: no-op
     assert f(FAKE, FAKE, FAKE, 4, 32, 256, 0, 16, path=7) == wq.WQ_ERR_INVALID_ARG
-    assert f(FAKE, FAKE, FAKE, 4, 32, 256, 0, 16, path=0x200) == wq.WQ_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, 4, 32, 256, 0, 16, path=0x400) == wq.WQ_ERR_INVALID_ARG
     assert f(FAKE, FAKE, FAKE, -1, 32, 256, 0, 16) == wq.WQ_ERR_INVALID_ARG
     assert f(FAKE, FAKE, FAKE, 4, 32, 256, 7, 16) == wq.WQ_ERR_INVALID_ARG
     assert f(FAKE, FAKE, FAKE, 4, 32, 256, 2, 64) == wq.WQ_ERR_UNSUPPORTED

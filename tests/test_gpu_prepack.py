@@ -26,17 +26,17 @@ def prepack_dev(p):
     return pre
 
 
-def run_pre(p, out="fp32", overlap=False, pre=None, **epi):
+def run_pre(p, out="fp32", overlap=False, pre=None, ready=False, **epi):
     A, _, _, _ = to_dev(p)
     pre = pre or prepack_dev(p)
-    C = wq.gemm_prepacked(A, pre, out_dtype=out, overlap=overlap, **epi)
+    C = wq.gemm_prepacked(A, pre, out_dtype=out, overlap=overlap, inputs_ready=ready, **epi)
     torch.cuda.synchronize()
     assert wq.wq_get_device_error() == wq.WQ_OK
     return C.float().cpu().numpy().astype(np.float64)
 
 
-def check_pre(p, out="fp32", overlap=False, what=""):
-    C = run_pre(p, out, overlap)
+def check_pre(p, out="fp32", overlap=False, what="", ready=False):
+    C = run_pre(p, out, overlap, ready=ready)
     Ce, S = oracle_ref(p)
     assert_parity(C, Ce, S, out, what)
     return C
@@ -62,25 +62,40 @@ def test_prepack_bytes_equal_oracle(fmt, N, K):
 
 
 # -- the GEMM on prepacked weights ------------------------------------------------
+# Two small-M kernels read the layout: the ring kernel (calls that declare
+# their inputs ready) and the staged kernel (dependent and plain calls).
+# WQ_GEMV_PRE_KERNEL forces one; the ring runs here with its inputs declared
+# ready, as it is launched in use.
+@pytest.fixture(params=["staged", "ring"])
+def kernel(request, monkeypatch):
+    monkeypatch.setenv("WQ_GEMV_PRE_KERNEL", request.param)
+    return request.param
+
+
+def ready_for(kernel):
+    return kernel == "ring"
+
+
 @pytest.mark.parametrize("fmt", ["int4", "nvfp4", "mxfp4"])
 @pytest.mark.parametrize("M", [1, 3, 8, 9, 16, 17, 40])
-def test_parity_against_oracle(fmt, M):
+def test_parity_against_oracle(fmt, M, kernel):
     p = synth.make_problem(fmt, M, 256, 1024, seed=M)
-    check_pre(p, "fp32" if M % 2 else "bf16", what=f"{fmt} M={M}")
+    check_pre(p, "fp32" if M % 2 else "bf16", what=f"{kernel} {fmt} M={M}", ready=ready_for(kernel))
 
 
 @pytest.mark.parametrize("fmt,N,K", [("int4", 200, 384), ("int4", 8, 128), ("nvfp4", 130, 544),
                                      ("nvfp4", 33, 160), ("mxfp4", 100, 2080), ("mxfp4", 5, 96)])
 @pytest.mark.parametrize("M", [1, 5, 16])
-def test_ragged_shapes(fmt, N, K, M):
+def test_ragged_shapes(fmt, N, K, M, kernel):
     """N not a multiple of 16; fp4 K not a multiple of 128 (a partial last
     block whose activation tail the kernel zeroes)."""
     p = synth.make_problem(fmt, M, N, K, seed=N + M)
-    check_pre(p, "fp32", what=f"{fmt} N={N} K={K} M={M}")
+    check_pre(p, "fp32", what=f"{kernel} {fmt} N={N} K={K} M={M}", ready=ready_for(kernel))
 
 
 @pytest.mark.parametrize("rb,wk", [("1", "0"), ("1", "3"), ("2", "1"), ("4", "2"), ("8", "1")])
-def test_cta_shapes(rb, wk, monkeypatch):
+def test_staged_cta_shapes(rb, wk, monkeypatch):
+    monkeypatch.setenv("WQ_GEMV_PRE_KERNEL", "staged")
     monkeypatch.setenv("WQ_GEMV_RB", rb)
     monkeypatch.setenv("WQ_GEMV_TMA_WK", wk)
     for fmt, M, N, K in (("int4", 1, 300, 3072), ("int4", 12, 200, 1024), ("nvfp4", 3, 130, 544),
@@ -103,41 +118,86 @@ def test_cta_shapes(rb, wk, monkeypatch):
         check_pre(p, "fp32", what=f"{fmt} rb={rb} wk={wk} M={M}")
 
 
+def _ring_smem(fmt, M, K, RB, Wk, P):
+    """Shared memory of a forced CTA shape of the ring kernel: the layout its
+    source documents (barriers, a ring of P slots per warp of RB code blocks
+    + the activation rows, the records, and the partial sums that alias
+    them)."""
+    r128 = lambda x: (x + 127) // 128 * 128  # noqa: E731
+    nk = -(-K // 128)
+    ipw = -(-nk // Wk)
+    P = min(P, ipw)
+    mrows = 16 if M > 8 else 8
+    Mc, MP = min(M, mrows), (16 if M > 8 else 8)
+    ring_off = r128(8 * Wk * P)
+    slot = r128(1024 * RB + 320 * Mc)
+    end = ring_off + Wk * P * slot + Wk * RB * ipw * (96 if fmt == "int4" else 512)
+    red = ring_off + Wk * MP * (RB * 16 + 4) * 4
+    return max(end, red) + 128
+
+
+@pytest.mark.parametrize("rb,wk,ring", [("1", "0", "3"), ("1", "3", "2"), ("2", "1", "3"), ("4", "2", "4"),
+                                        ("4", "0", "1"), ("2", "3", "5")])
+def test_ring_cta_shapes(rb, wk, ring, monkeypatch):
+    """Every forced shape of the ring kernel (row blocks per CTA, warps, ring
+    slots) computes the product; a shape above 227 KB of shared memory is
+    refused."""
+    monkeypatch.setenv("WQ_RING_RB", rb)
+    monkeypatch.setenv("WQ_RING_WK", wk)
+    monkeypatch.setenv("WQ_RING_P", ring)
+    for fmt, M, N, K in (("int4", 1, 300, 3072), ("int4", 12, 200, 1024), ("nvfp4", 3, 130, 544),
+                         ("mxfp4", 16, 100, 2080), ("nvfp4", 2, 40, 16384)):
+        p = synth.make_problem(fmt, M, N, K, seed=int(rb) * 10 + int(wk) + M)
+        if _ring_smem(fmt, M, K, int(rb), 1 << int(wk), int(ring)) > 227 * 1024:
+            with pytest.raises(wq.WQError) as e:
+                run_pre(p, "fp32", ready=True)
+            assert e.value.status == wq.WQ_ERR_UNSUPPORTED
+            continue
+        check_pre(p, "fp32", what=f"{fmt} rb={rb} wk={wk} ring={ring} M={M}", ready=True)
+
+
+def test_ring_shape_refusal_is_reachable():
+    """The shape table above really contains a refused case (fp4 records of
+    16384 k in one warp of 4 row blocks)."""
+    assert _ring_smem("nvfp4", 2, 16384, 4, 1, 1) > 227 * 1024
+    assert _ring_smem("int4", 1, 3072, 2, 2, 3) < 64 * 1024
+
+
 @pytest.mark.parametrize("M", [3, 16])
-def test_int4_zero_points_above_128(M):
+def test_int4_zero_points_above_128(M, kernel):
     p = synth.make_problem("int4", M, 144, 1024, seed=M + 7)
     rng = np.random.default_rng(M)
     z = p["zeros"].copy()
     big = rng.random(z.shape) < 0.3
     z[big] = rng.integers(129, 256, size=int(big.sum()), dtype=np.uint8)
     p["zeros"] = z
-    check_pre(p, "fp32", what=f"int4 big zeros M={M}")
+    check_pre(p, "fp32", what=f"{kernel} int4 big zeros M={M}", ready=ready_for(kernel))
 
 
 @pytest.mark.parametrize("M", [3, 16])
-def test_mxfp4_scales_above_2_pow_15(M):
+def test_mxfp4_scales_above_2_pow_15(M, kernel):
     p = synth.make_problem("mxfp4", M, 144, 1024, seed=M + 9)
     rng = np.random.default_rng(M)
     E = p["scales"].copy()
     big = rng.random(E.shape) < 0.3
     E[big] = rng.integers(143, 161, size=int(big.sum()), dtype=np.uint8)
     p["scales"] = E
-    check_pre(p, "fp32", what=f"mxfp4 E>142 M={M}")
+    check_pre(p, "fp32", what=f"{kernel} mxfp4 E>142 M={M}", ready=ready_for(kernel))
 
 
 @pytest.mark.parametrize("M", [4, 16])
-def test_int4_codes_equal_zero_give_zero(M):
+def test_int4_codes_equal_zero_give_zero(M, kernel):
     N, K, g = 96, 512, 128
     rng = np.random.default_rng(5)
     z = rng.integers(0, 16, size=(N, K // g), dtype=np.uint8)
     codes = np.repeat(z, g, axis=1)
     p = synth.make_problem("int4", M, N, K, seed=5)
     p.update(packed=(codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8), zeros=z)
-    assert np.all(run_pre(p, "fp32") == 0)
+    assert np.all(run_pre(p, "fp32", ready=ready_for(kernel)) == 0)
 
 
 @pytest.mark.parametrize("fmt", ["int4", "nvfp4"])
-def test_one_hot_activation_selects_weight(fmt):
+def test_one_hot_activation_selects_weight(fmt, kernel):
     """a[m, k] = 1 at one k per row: C[m, n] = w[n, k] exactly (fp32 out)."""
     N, K = 64, 512
     p = synth.make_problem(fmt, 16, N, K, seed=11)
@@ -146,7 +206,7 @@ def test_one_hot_activation_selects_weight(fmt):
     A[np.arange(16), ks] = 1.0
     p["A"] = synth.bf16_bits(A)
     W64, _ = oracle.dequant(p["packed"], p["scales"], p["zeros"], fmt, p["group"])
-    C = run_pre(p, "fp32")
+    C = run_pre(p, "fp32", ready=ready_for(kernel))
     assert np.array_equal(C, W64[:, ks].T)
 
 
@@ -157,6 +217,55 @@ def test_deterministic_and_overlap_equal():
     C2 = run_pre(p, "fp32", pre=pre)
     C3 = run_pre(p, "fp32", overlap=True, pre=pre)
     assert np.array_equal(C1, C2) and np.array_equal(C1, C3)
+
+
+def test_ring_deterministic_across_launch_flags(monkeypatch):
+    """The ring kernel with a forced shape gives the same bits whether it is
+    launched plain, overlapped or with its inputs declared ready."""
+    monkeypatch.setenv("WQ_GEMV_PRE_KERNEL", "ring")
+    monkeypatch.setenv("WQ_RING_RB", "2")
+    monkeypatch.setenv("WQ_RING_WK", "1")
+    p = synth.make_problem("int4", 16, 1024, 3072, seed=9)
+    pre = prepack_dev(p)
+    C1 = run_pre(p, "fp32", pre=pre)
+    C2 = run_pre(p, "fp32", pre=pre, ready=True)
+    C3 = run_pre(p, "fp32", pre=pre, overlap=True)
+    C4 = run_pre(p, "fp32", pre=pre, ready=True)
+    assert np.array_equal(C1, C2) and np.array_equal(C1, C3) and np.array_equal(C2, C4)
+
+
+def test_inputs_ready_chain():
+    """A chain of calls with WQ_LAUNCH_INPUTS_READY (activations written
+    before the chain, distinct weights, M = 1, 4, 16 in turn, then dependent
+    calls and a plain torch consumer): each call completes in stream order,
+    so every output read after the chain is complete and oracle-green."""
+    N, K = 1024, 3072
+    ps = [synth.make_problem("int4", M, N, K, seed=70 + i) for i, M in enumerate((1, 4, 16, 1, 4, 16))]
+    pres = [prepack_dev(p) for p in ps]
+    As = [to_dev(p)[0] for p in ps]
+    torch.cuda.synchronize()
+    outs = []
+    for A, pre in zip(As, pres):
+        outs.append(wq.gemm_prepacked(A, pre, inputs_ready=True))
+    # a dependent call that reads the last ready call's output as its input
+    p2 = synth.make_problem("int4", 16, N, N, seed=79)
+    pre2 = prepack_dev(p2)
+    torch.cuda.synchronize()
+    outs2 = []
+    for A, pre in zip(As, pres):
+        outs2.append(wq.gemm_prepacked(A, pre, inputs_ready=True))
+    y = wq.gemm_prepacked(outs2[-1], pre2, overlap=True)
+    total = sum(o.float().sum() for o in outs2)   # a plain stream consumer of every output
+    torch.cuda.synchronize()
+    assert wq.wq_get_device_error() == wq.WQ_OK
+    for p, o, o2 in zip(ps, outs, outs2):
+        Ce, S = oracle_ref(p)
+        assert_parity(o.float().cpu().numpy().astype(np.float64), Ce, S, "bf16", "ready chain")
+        assert torch.equal(o, o2)
+    a_bits = outs2[-1].view(torch.int16).cpu().numpy().view(np.uint16)
+    Ce, S = oracle_ref(dict(p2, A=a_bits))
+    assert_parity(y.float().cpu().numpy().astype(np.float64), Ce, S, "bf16", "dependent after ready chain")
+    assert float(total) == float(sum(o.float().sum() for o in outs2))
 
 
 def test_overlapped_launches_chain_correctly():
@@ -179,11 +288,11 @@ def test_overlapped_launches_chain_correctly():
 
 
 @pytest.mark.parametrize("M,K", [(16, 8192), (16, 16384), (5, 16384), (1, 16384)])
-def test_long_rows(M, K):
+def test_long_rows(M, K, kernel):
     """K up to the kernel's limit; 16 activation rows of K = 8192 do not fit
     beside the weights, so the call takes CTAs of fewer rows."""
     p = synth.make_problem("int4", M, 96, K, seed=K + M)
-    check_pre(p, "fp32", what=f"K={K} M={M}")
+    check_pre(p, "fp32", what=f"{kernel} K={K} M={M}", ready=ready_for(kernel))
 
 
 def test_k_above_limit_is_unsupported():
@@ -197,26 +306,27 @@ def test_k_above_limit_is_unsupported():
 
 @pytest.mark.parametrize("fmt", ["int4", "nvfp4", "mxfp4"])
 @pytest.mark.parametrize("M", [1, 16, 40])
-def test_fused_epilogue(fmt, M):
+def test_fused_epilogue(fmt, M, kernel):
     p = synth.make_problem(fmt, M, 256, 1024, seed=M + 3)
     rng = np.random.default_rng(M)
     bias = synth.bf16_bits((rng.normal(size=256) * 0.5).astype(np.float32))
     res = synth.bf16_bits(rng.normal(size=(M, 128)).astype(np.float32))
     dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
     out = "fp32" if M % 2 else "bf16"
-    Y = run_pre(p, out, bias=dev(bias), residual=dev(res), gated=True)
+    Y = run_pre(p, out, bias=dev(bias), residual=dev(res), gated=True, ready=ready_for(kernel))
     C, S = oracle.gemm(p["A"], p["packed"], p["scales"], p["zeros"], fmt, p["group"])
     Ye, T = oracle.epilogue(C, S, bias, res, True, out)
     assert not (np.abs(Y - Ye) > T).any()
 
 
 @pytest.mark.parametrize("M", [1, 4, 16])
-def test_decode_workload_full_size(M):
+def test_decode_workload_full_size(M, kernel):
     """The decode configuration (int4 g128, N = 8192, K = 3072, bf16 out) in
-    the launch configuration the bench times (overlap on): oracle on sampled
-    columns (all rows)."""
+    the launch configurations the bench times (the ring kernel with its
+    inputs ready, the staged kernel overlapped): oracle on sampled columns
+    (all rows)."""
     p = synth.workload_problem("decode_int4", M=M, seed=3)
-    C = run_pre(p, "bf16", overlap=True)
+    C = run_pre(p, "bf16", overlap=True, ready=ready_for(kernel))
     cols = sample(p["N"], 96, M)
     Ce, S = oracle_ref(p, cols=cols)
     assert_parity(C[:, cols], Ce, S, "bf16", f"decode M={M}")

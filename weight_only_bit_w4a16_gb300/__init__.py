@@ -204,13 +204,18 @@ def workspace(M, N, K, fmt, group=None, device=None):
     return ws
 
 
+def _launch_bits(overlap, inputs_ready):
+    return (WQ_LAUNCH_OVERLAP if overlap else 0) | (WQ_LAUNCH_INPUTS_READY if inputs_ready else 0)
+
+
 def gemm(A, packed, scales, zeros, fmt, group=None, out_dtype="bf16", out=None, path="auto", stream=None,
-         overlap=False, workspace=None, bias=None, residual=None, gated=False):
+         overlap=False, workspace=None, bias=None, residual=None, gated=False, inputs_ready=False):
     """C = A . deq(packed, scales, zeros)^T on A's device and current stream.
 
     overlap=True sets WQ_LAUNCH_OVERLAP (programmatic dependent launch): the
     caller guarantees the preceding kernel on the stream does not write the
-    weights.  workspace: a zeroed uint8 CUDA tensor (see workspace()) that
+    weights.  inputs_ready=True sets WQ_LAUNCH_INPUTS_READY: A, too, is
+    written by no kernel that may still be running (include/wq.h).  workspace: a zeroed uint8 CUDA tensor (see workspace()) that
     lets the tensor-core path split tiles over the SMs; "auto" takes the
     cached one.  bias (N,) bf16, residual (M, outputs) bf16 and gated select
     the fused epilogue of wq_gemm_fused (gated: C has N / 2 columns).
@@ -242,7 +247,7 @@ def gemm(A, packed, scales, zeros, fmt, group=None, out_dtype="bf16", out=None, 
                               or not t.is_contiguous()):
             raise ValueError(f"bias / residual must be contiguous bf16 CUDA tensors of shape {shape}")
     fmt_word = f | (WQ_OUT_F32 if odt == torch.float32 else 0)
-    pcode = (PATHS[path] if isinstance(path, str) else int(path)) | (WQ_LAUNCH_OVERLAP if overlap else 0)
+    pcode = (PATHS[path] if isinstance(path, str) else int(path)) | _launch_bits(overlap, inputs_ready)
     if isinstance(workspace, str) and workspace == "auto":
         workspace = globals()["workspace"](M, N, K, fmt, group, A.device)
     if bias is not None or residual is not None or gated:
@@ -302,7 +307,7 @@ def prepack(packed, scales, zeros, fmt, group=None, stream=None, out=None) -> Pr
 
 
 def gemm_prepacked(A, pre: Prepacked, out_dtype="bf16", out=None, stream=None, overlap=False, bias=None,
-                   residual=None, gated=False, path="auto", workspace=None):
+                   residual=None, gated=False, path="auto", workspace=None, inputs_ready=False):
     """C = A . deq(B)^T for a prepacked weight (wq_gemm_prepacked); the other
     arguments as for gemm()."""
     import torch
@@ -330,7 +335,7 @@ def gemm_prepacked(A, pre: Prepacked, out_dtype="bf16", out=None, stream=None, o
         epi = ctypes.byref(wq_epilogue(None if bias is None else bias.data_ptr(),
                                        None if residual is None else residual.data_ptr(), 1 if gated else 0))
     fmt_word = _fmt(pre.fmt) | (WQ_OUT_F32 if odt == torch.float32 else 0)
-    pcode = (PATHS[path] if isinstance(path, str) else int(path)) | (WQ_LAUNCH_OVERLAP if overlap else 0)
+    pcode = (PATHS[path] if isinstance(path, str) else int(path)) | _launch_bits(overlap, inputs_ready)
     if isinstance(workspace, str) and workspace == "auto":
         workspace = globals()["workspace"](M, N, K, pre.fmt, pre.group, A.device)
     if workspace is not None and (not workspace.is_cuda or workspace.dtype != torch.uint8):

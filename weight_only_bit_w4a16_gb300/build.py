@@ -15,7 +15,7 @@ LIB = os.path.join(HERE, "libwq.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["wq_api.cu", "wq_dequant.cu", "wq_gemv.cu", "wq_gemv_tma.cu", "wq_tc.cu", "wq_prepack.cu",
-           "wq_gemv_pre.cu"]
+           "wq_gemv_pre.cu", "wq_gemv_staged.cu"]
 HEADERS = ["wq_common.cuh", "wq_gemv.cuh", "wq_internal.h", "wq_tc.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -44,8 +44,9 @@ int gemm_impl(const void* A, const uint8_t* packed, const void* scales, const ui
     const int fmt = format & 0xFF;
     const bool out_f32 = (format & WQ_OUT_F32) != 0;
     if (M < 0) return WQ_ERR_INVALID_ARG;
-    if (path & ~(0xFF | WQ_LAUNCH_OVERLAP)) return WQ_ERR_INVALID_ARG;
-    const bool overlap = (path & WQ_LAUNCH_OVERLAP) != 0;
+    if (path & ~(0xFF | WQ_LAUNCH_OVERLAP | WQ_LAUNCH_INPUTS_READY)) return WQ_ERR_INVALID_ARG;
+    const bool inputs_ready = (path & WQ_LAUNCH_INPUTS_READY) != 0;
+    const bool overlap = (path & WQ_LAUNCH_OVERLAP) != 0 || inputs_ready;
     path &= 0xFF;
     if (path != WQ_PATH_AUTO && path != WQ_PATH_GEMV && path != WQ_PATH_TC) return WQ_ERR_INVALID_ARG;
     if (workspace_bytes > 0 && !workspace) return WQ_ERR_INVALID_ARG;
@@ -76,7 +77,7 @@ int gemm_impl(const void* A, const uint8_t* packed, const void* scales, const ui
         if (st != WQ_ERR_UNSUPPORTED) return st;
         // shapes the tensor-core kernel does not take run on the GEMV kernel
     }
-    return wq::launch_gemv(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, overlap, epi, s);
+    return wq::launch_gemv(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, overlap, inputs_ready, epi, s);
 }
 
 }  // namespace
@@ -214,7 +215,8 @@ WQ_EXPORT int wq_get_device_error(void) {
     const int a = wq::read_and_clear_device_status();
     const int b = wq::read_and_clear_gemv_status();
     const int c = wq::read_and_clear_pre_status();
-    return a != 0 ? a : (b != 0 ? b : c);
+    const int d = wq::read_and_clear_staged_status();
+    return a != 0 ? a : (b != 0 ? b : (c != 0 ? c : d));
 }
 
 WQ_EXPORT int wq_selftest_timeout(void* stream) {

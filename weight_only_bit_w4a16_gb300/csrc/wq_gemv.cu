@@ -539,15 +539,19 @@ int launch_inst(const GemvArgs& args, dim3 grid, int threads, size_t smem, int c
 }  // namespace
 
 int launch_gemv(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C,
-                int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, const Epilogue& epi,
-                cudaStream_t stream) {
+                int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, bool inputs_ready,
+                const Epilogue& epi, cudaStream_t stream) {
+    // the register-streaming kernels below read A after the dependency wait
+    // whatever the caller declared, which is always correct
+    if (inputs_ready) pdl = true;
     if (M == 0 || N == 0) return WQ_OK;
     // WQ_GEMV_KERNEL=split|cluster (tests, tuning) skips the streaming kernel
     const char* force = getenv("WQ_GEMV_KERNEL");
     const bool force_cluster = getenv("WQ_GEMV_FORCE_CLUSTER") || (force && !strcmp(force, "cluster"));
     const bool force_split = force && !strcmp(force, "split");
     if (!force_cluster && !force_split) {
-        const int st = launch_gemv_tma(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, pdl, epi, stream);
+        const int st = launch_gemv_tma(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, pdl, inputs_ready,
+                                       epi, stream);
         if (st != WQ_ERR_UNSUPPORTED) return st;
     }
     int dev = 0, sms = 148;

@@ -1,31 +1,45 @@
 // wq_gemv_pre.cu -- the small-M kernel for weights in the prepacked layout
 // (wq_prepack.cu; definition above wq_prepack_bytes in include/wq.h).
 //
-// Same work split and arithmetic as the streaming kernel (wq_gemv_tma.cu):
-// a CTA takes rb blocks of 16 weight rows x all of K, each block's K split
-// over Wk warps; the weights are the M operand of mma.sync.m16n8k16 and the
-// activations its N = 8 operand; int4 g128 runs the MMAs on the exact
-// integers (code - zero) and scales the fp32 partial sums per iteration.
-// What the layout changes is everything around the loop:
-//   - per warp, its codes are ONE bulk copy (nit contiguous 1024-byte
-//     blocks) and, for int4, its decode records a second one (nit x 96
-//     bytes, already in the form the loop reads): no scale loads, no record
-//     decode, no row padding;
-//   - the activations need no permutation (a lane's four words of a block
-//     are the natural k units c + 4j), so after the dependency wait the first
-//     warp of each K range copies them with one bulk copy per row and the
-//     other warps of the range wait on that copy's mbarrier: no register
-//     round trip and no named barrier.
+// Arithmetic as in the streaming kernel (wq_gemv_tma.cu): the weights are
+// the M operand of mma.sync.m16n8k16 and the activations its N = 8 operand;
+// int4 g128 runs the MMAs on the exact integers (code - zero) and scales the
+// fp32 partial sums per 128-k block; fp4 weights are decoded with their
+// scale (exact in bf16).
+//
+// Work split.  A CTA takes up to RB blocks of 16 weight rows x all of K; its
+// Wk warps split K into equal ranges, and each warp runs its range for ALL of
+// the CTA's row blocks, so an activation fragment read from shared memory
+// feeds RB row blocks and the CTA fetches each activation byte once.
+//
+// Data movement.  Nothing is staged whole: every warp streams its range
+// through a ring of P slots.  The slot of step t (k-block it0 + t) holds the
+// RB code blocks of that k-block (1024 bytes each) and its activation slice
+// (Mc rows x 128 k).  The lanes fill a slot with 16-byte cp.async copies and
+// then arrive (without a count increment) on the slot's mbarrier, an arrival
+// that happens once their copies have landed; a phase of 32 arrivals
+// therefore means the whole slot is in shared memory.  The warp refills the
+// slot with step t + P once step t's MMAs are done.  The int4 decode records
+// of the warp's range (96 bytes per block, already in the form the loop
+// reads) are copied once, ahead of step 0.  The small CTA footprint lets the
+// CTAs of several consecutive calls share an SM, so that one call's weights
+// stream while another's decode runs.
+//
+// Dependencies (programmatic dependent launch).  The code blocks of the first
+// P steps are requested at once; the activation copies wait for the
+// preceding kernel, unless the caller declared A complete already
+// (inputs_ready), in which case the kernel waits only before storing C.
 //
 // Shared memory (from a 128-byte aligned base):
-//   bars  [warps] u64 at 0, [Wk] u64 at 128   codes / activations landed
-//   W     [warps][ipw][1024]                  the warps' code blocks
-//   A     [Mc][SA]                            activation rows, natural order
-//   R     [warps][ipw][96]  int4              the copied record blocks
-//         [warps][ipw][512] fp4               decoded multipliers, per lane
-//   red   [Wk][MP][rows + 4] f32 at 256       partial sums (aliases W, A, R)
+//   bars  [Wk][P] u64 at 0                     slot landed (32 arrivals)
+//   ring  [Wk][P][slot_bytes] at ring_off      RB code blocks, then the
+//                                              activation rows, kAStride apart
+//   recs  [Wk][RB][ipw][96]  int4 at rec_off   the copied record blocks
+//         [Wk][RB][ipw][512] fp4               decoded multipliers, per lane
+//   red   [Wk][MP][RB*16 + 4] f32 at ring_off  partial sums (aliases ring/recs)
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -52,10 +66,10 @@ namespace {
 using namespace gemv;
 using namespace sm100;
 
-constexpr int kMaxIpw = 16;                             // 128-k blocks per warp
-constexpr int kMaxWkLog2 = 3;                           // warps per K split <= 8
 constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s: far above any legal wait
-constexpr uint32_t kBarBytes = 256;
+constexpr int kMaxWkLog2 = 3;                           // K ranges (warps) per CTA <= 8
+constexpr uint32_t kAStride = 320;   // activation row stride in a slot: 256 + 64, so that the
+                                     // rows a quarter-warp reads sit in opposite bank halves
 
 struct PreArgs {
     const uint8_t* codes;   // code blocks
@@ -65,10 +79,12 @@ struct PreArgs {
     int M, N, K;
     int I, Nb;              // 128-k blocks per row, 16-row blocks
     int out_f32;
-    int mrows;              // activation rows per CTA (16, 8, 4, 2 or 1)
-    int rb, wk_log2, ipw;
-    uint32_t SA;            // shared row stride of the activations (bytes)
-    uint32_t w_off, a_off, r_off, red_off;
+    int mrows;              // activation rows per CTA (16 or 8)
+    int ipw;                // k-blocks per warp (its K range)
+    int P;                  // ring slots per warp
+    uint32_t slot_bytes;    // RB x 1024 + activation rows x kAStride (128-aligned)
+    uint32_t ring_off, rec_off;
+    int wide;               // grid x Nb does not fit 32 bits
     int inputs_ready;       // A may be read before the preceding kernel completes
     Epilogue epi;
 };
@@ -81,8 +97,15 @@ __device__ __forceinline__ uint32_t lds32(uint32_t saddr) {
     return v;
 }
 
-__device__ __forceinline__ void sts128_zero(uint32_t saddr) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(saddr), "r"(0) : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// copies `bytes` (0 or 16) and zero-fills the rest of the 16-byte unit
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // The lane's four words of one 128-k block, rows r (qa) and r + 8 (qb), in
@@ -94,251 +117,389 @@ __device__ __forceinline__ void block_words(uint32_t wp, uint4& qa, uint4& qb) {
     qb = make_uint4(b0.x, b0.y, b1.x, b1.y);
 }
 
-// int4 g128 loop.  rp: the lane's record pair {row r, row r + 8} (4 bytes
-// each: bf16 scale | bf16 (128 + min(z, 128)) << 16); rq: the pair of second
-// subtrahends (2 bytes each, read only when some zero point exceeds 128).
+// One warp's stream: step t (k-block it0 + t) lands in slot t mod P.
+template <int RB>
+struct Ring {
+    uint32_t slots;           // slot 0 (shared address)
+    uint32_t bar;             // barrier of slot 0 (8 bytes per slot)
+    uint32_t slot_bytes;
+    const uint8_t* codes;     // code block (bs, it0) in global memory
+    size_t row_stride;        // bytes between the blocks of consecutive row blocks (I x 1024)
+    const uint16_t* asrc;     // the lane's first activation unit: row mz + (lane >> 4), k = it0 * 128 + 8 (lane & 15)
+    const uint16_t* azero;    // a valid address for the zero-filled units (no byte is read there)
+    size_t lda2;              // two activation rows (2 K elements)
+    int krem;                 // k left in the row from it0 * 128, minus 8 (lane & 15)
+    uint32_t adst;            // the lane's first unit in a slot's activation rows
+    int aunits;               // 16-byte units the lane copies per step: rows lane >> 4, + 2, ... < Mc
+    int nb, nit, P, lane;
+
+    __device__ __forceinline__ void issue_codes(int t, int slot) const {
+        const uint32_t d = slots + slot_bytes * slot + 16u * lane;
+        const uint8_t* g = codes + (size_t)t * 1024 + 16 * lane;
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+            if (q < nb) {
+                cp_async16(d + 1024u * q, g + row_stride * q);
+                cp_async16(d + 1024u * q + 512, g + row_stride * q + 512);
+            }
+        }
+    }
+    // the activation slice of step t (16-byte units past K zero-filled: K is
+    // a multiple of 32, so a unit is wholly inside or outside), then the
+    // lane's arrival on the slot's barrier, which covers every copy the lane
+    // issued before it
+    __device__ __forceinline__ void issue_acts(int t, int slot) const {
+        uint32_t d = slots + slot_bytes * slot + adst;
+        const bool in = t * 128 < krem;
+        const uint16_t* g = in ? asrc + t * 128 : azero;
+        const uint32_t bytes = in ? 16u : 0u;
+        for (int v = 0; v < aunits; ++v) {
+            cp_async16_zfill(d, g, bytes);
+            d += 2 * kAStride;
+            if (in) g += lda2;
+        }
+        cp_async_arrive_noinc(bar + 8u * slot);
+    }
+    // wait for the slot whose current phase has parity ph; ties sb to the
+    // wait so that the compiler cannot hoist the slot's shared loads above it
+    __device__ __forceinline__ bool wait(int slot, uint32_t ph, uint32_t& sb) const {
+        const bool ok = mbar_wait_sleep(bar + 8u * slot, ph, kWaitNs);
+        asm volatile("" : "+r"(sb)::"memory");
+        return ok;
+    }
+    // after a failed wait: let the steps still in flight, [from, upto), land
+    // (bounded) before the CTA's shared memory can be reused
+    __device__ __forceinline__ void drain(int from, int upto) const {
+        for (int j = from; j < upto; ++j) {
+            uint32_t dummy = 0;
+            if (!wait(j % P, (uint32_t)(j / P) & 1u, dummy)) break;
+        }
+    }
+};
+
+// Every shared load of a step's slot feeds an MMA whose result ends up in
+// the accumulators; this volatile asm needs them, so the compiler has the
+// step's loads and MMAs done before it, and therefore before the refill
+// copies that follow it.
+template <int RB, int NT>
+__device__ __forceinline__ void slot_consumed(float (&acc)[RB][NT][4]) {
+#pragma unroll
+    for (int q = 0; q < RB; ++q)
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+            asm volatile("" ::"f"(acc[q][t][0]), "f"(acc[q][t][1]), "f"(acc[q][t][2]), "f"(acc[q][t][3])
+                         : "memory");
+    __syncwarp();
+}
+
+// int4 g128, one row block of a step.  rec: its record block; the lane's
+// record pair {row r, row r + 8} (4 bytes each: bf16 scale | bf16 (128 +
+// min(z, 128)) << 16) sits at rec + 8 r, the pair of second subtrahends (2
+// bytes each, read only when some zero point exceeds 128) at rec + 64 + 4 r.
 template <int NT, bool TWO>
-__device__ __forceinline__ void loop_int4(uint32_t wp, uint32_t rp, uint32_t rq, uint32_t (&ap)[NT], int nit,
+__device__ __forceinline__ void step_int4(uint32_t wp, uint32_t rec, uint32_t r, const uint4 (&bv)[NT][4],
                                           float (&acc)[NT][4]) {
-    // the rare second-subtrahend instance runs unrolled once (register cap)
-#pragma unroll(TWO ? 1 : 2)
-    for (int i = 0; i < nit; ++i) {
-        uint4 qa, qb;
-        block_words(wp, qa, qb);
-        const uint2 rr = lds64(rp);
-        uint32_t zA2 = 0, zB2 = 0;
-        if constexpr (TWO) {
-            const uint32_t q = lds32(rq);
-            zA2 = splat16(q);
-            zB2 = splat16(q >> 16);
-        }
-        it_int4<NT, TWO>(qa, qb, ap, acc, prmt(rr.x, rr.x, 0x3232u), zA2, prmt(rr.y, rr.y, 0x3232u), zB2,
-                         __uint_as_float(rr.x << 16), __uint_as_float(rr.y << 16));
-        wp += 1024;
-        rp += 96;
-        rq += 96;
+    uint4 qa, qb;
+    block_words(wp, qa, qb);
+    const uint2 rr = lds64(rec + 8u * r);
+    uint32_t zzA2 = 0, zzB2 = 0;
+    if constexpr (TWO) {
+        const uint32_t q = lds32(rec + 64u + 4u * r);
+        zzA2 = splat16(q);
+        zzB2 = splat16(q >> 16);
+    }
+    const uint32_t zzA = prmt(rr.x, rr.x, 0x3232u), zzB = prmt(rr.y, rr.y, 0x3232u);
+    const float sa = __uint_as_float(rr.x << 16), sb = __uint_as_float(rr.y << 16);
+    const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w}, wb[4] = {qb.x, qb.y, qb.z, qb.w};
+    // CH independent MMA chains per tile (words j = h mod CH): with one tile
+    // two chains keep the dependent sequence 4 deep; two tiles already are
+    // two chains
+    constexpr int CH = NT == 1 ? 2 : 1;
+    float part[CH][NT][4];
 #pragma unroll
-        for (int t = 0; t < NT; ++t) ap[t] += 256;
+    for (int j = 0; j < 4; ++j) {
+        uint32_t pa[4], pb[4];
+        int4_word_kk4<TWO>(wa[j], zzA, zzA2, pa);
+        int4_word_kk4<TWO>(wb[j], zzB, zzB2, pb);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            if (j < CH) mma16816_z(part[j % CH][t], pa[0], pb[0], pa[1], pb[1], bv[t][j].x, bv[t][j].y);
+            else mma16816(part[j % CH][t], pa[0], pb[0], pa[1], pb[1], bv[t][j].x, bv[t][j].y);
+            mma16816(part[j % CH][t], pa[2], pb[2], pa[3], pb[3], bv[t][j].z, bv[t][j].w);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float p = part[0][t][e];
+            if constexpr (CH == 2) p += part[CH - 1][t][e];
+            acc[t][e] = fmaf(e < 2 ? sa : sb, p, acc[t][e]);
+        }
     }
 }
 
-// fp4 loop.  rp: the lane's decoded multipliers, words j = 0..3 of row r
-// (16 bytes) then of row r + 8; the second multipliers (MXFP4 scales above
-// 2^15) 256 bytes on.
+// fp4, one row block of a step.  rp: the lane's decoded multipliers, words
+// j = 0..3 of row r (16 bytes) then of row r + 8; the second multipliers
+// (MXFP4 scales above 2^15) 256 bytes on.
 template <int NT, bool TWO>
-__device__ __forceinline__ void loop_fp4(uint32_t wp, uint32_t rp, uint32_t (&ap)[NT], int nit, float (&acc)[NT][4]) {
-#pragma unroll 2
-    for (int i = 0; i < nit; ++i) {
-        uint4 qa, qb;
-        block_words(wp, qa, qb);
-        const uint4 ma = lds128(rp), mb = lds128(rp + 16);
-        uint4 na = make_uint4(0, 0, 0, 0), nb = na;
-        if constexpr (TWO) {
-            na = lds128(rp + 256);
-            nb = lds128(rp + 272);
-        }
-        const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w}, wb[4] = {qb.x, qb.y, qb.z, qb.w};
-        const uint32_t mua[4] = {ma.x, ma.y, ma.z, ma.w}, mub[4] = {mb.x, mb.y, mb.z, mb.w};
-        const uint32_t m2a[4] = {na.x, na.y, na.z, na.w}, m2b[4] = {nb.x, nb.y, nb.z, nb.w};
+__device__ __forceinline__ void step_fp4(uint32_t wp, uint32_t rp, const uint4 (&bv)[NT][4], float (&acc)[NT][4]) {
+    uint4 qa, qb;
+    block_words(wp, qa, qb);
+    const uint4 ma = lds128(rp), mb = lds128(rp + 16);
+    uint4 na = make_uint4(0, 0, 0, 0), nb = na;
+    if constexpr (TWO) {
+        na = lds128(rp + 256);
+        nb = lds128(rp + 272);
+    }
+    const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w}, wb[4] = {qb.x, qb.y, qb.z, qb.w};
+    const uint32_t mua[4] = {ma.x, ma.y, ma.z, ma.w}, mub[4] = {mb.x, mb.y, mb.z, mb.w};
+    const uint32_t m2a[4] = {na.x, na.y, na.z, na.w}, m2b[4] = {nb.x, nb.y, nb.z, nb.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t pa[4], pb[4];
-            e2m1_word_raw(wa[j], pa);
-            e2m1_word_raw(wb[j], pb);
+    for (int j = 0; j < 4; ++j) {
+        uint32_t pa[4], pb[4];
+        e2m1_word_raw(wa[j], pa);
+        e2m1_word_raw(wb[j], pb);
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                pa[s] = bf16x2_mul(pa[s], mua[j]);
-                pb[s] = bf16x2_mul(pb[s], mub[j]);
-                if constexpr (TWO) {
-                    pa[s] = bf16x2_mul(pa[s], m2a[j]);
-                    pb[s] = bf16x2_mul(pb[s], m2b[j]);
-                }
-            }
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                const uint4 bv = lds128(ap[t] + 64 * j);
-                mma16816(acc[t], pa[0], pb[0], pa[1], pb[1], bv.x, bv.y);
-                mma16816(acc[t], pa[2], pb[2], pa[3], pb[3], bv.z, bv.w);
+        for (int s = 0; s < 4; ++s) {
+            pa[s] = bf16x2_mul(pa[s], mua[j]);
+            pb[s] = bf16x2_mul(pb[s], mub[j]);
+            if constexpr (TWO) {
+                pa[s] = bf16x2_mul(pa[s], m2a[j]);
+                pb[s] = bf16x2_mul(pb[s], m2b[j]);
             }
         }
-        wp += 1024;
-        rp += 512;
 #pragma unroll
-        for (int t = 0; t < NT; ++t) ap[t] += 256;
+        for (int t = 0; t < NT; ++t) {
+            mma16816(acc[t], pa[0], pb[0], pa[1], pb[1], bv[t][j].x, bv[t][j].y);
+            mma16816(acc[t], pa[2], pb[2], pa[3], pb[3], bv[t][j].z, bv[t][j].w);
+        }
     }
 }
 
-template <int FMT, int NT, bool EPI>
-__global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_pre_kernel(const PreArgs a) {
+// The warp's whole range, step by step as the slots land: every row block of
+// the step, then the refill of the slot.  Returns false if a copy never
+// landed (the ones still in flight are drained first).
+//   lane_w : the lane's weight offset in a code block
+//   aoff   : the lane's activation offset in a slot, per MMA tile
+//   rlane  : the lane's offset in a record block (int4: its row r)
+template <int FMT, int NT, int RB, bool TWO>
+__device__ __forceinline__ bool run_range(const Ring<RB>& ring, uint32_t lane_w, const uint32_t (&aoff)[NT],
+                                       uint32_t rslice, uint32_t rlane, int ipw, float (&acc)[RB][NT][4]) {
+    constexpr uint32_t kRec = FMT == kINT4 ? 96 : 512;
+    int slot = 0;
+    uint32_t ph = 0;
+    for (int i = 0; i < ring.nit; ++i) {
+        uint32_t sb = ring.slots + ring.slot_bytes * slot;
+        if (!ring.wait(slot, ph, sb)) {
+            ring.drain(i + 1, min(ring.nit, i + ring.P));
+            return false;
+        }
+        // the step's activation fragments, read once for all its row blocks
+        uint4 bv[NT][4];
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) bv[t][j] = lds128(sb + aoff[t] + 64 * j);
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+            if (q < ring.nb) {
+                const uint32_t rec = rslice + (uint32_t)(q * ipw + i) * kRec;
+                if constexpr (FMT == kINT4) step_int4<NT, TWO>(sb + 1024u * q + lane_w, rec, rlane, bv, acc[q]);
+                else step_fp4<NT, TWO>(sb + 1024u * q + lane_w, rec + rlane, bv, acc[q]);
+            }
+        }
+        slot_consumed<RB, NT>(acc);
+        if (i + ring.P < ring.nit) {
+            ring.issue_codes(i + ring.P, slot);
+            ring.issue_acts(i + ring.P, slot);
+        }
+        if (++slot == ring.P) {
+            slot = 0;
+            ph ^= 1u;
+        }
+    }
+    return true;
+}
+
+template <int FMT, int NT, bool EPI, int RB>
+__global__ void __launch_bounds__(256, NT == 1 ? 3 : 2) gemv_pre_kernel(const PreArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 127u) & ~127u;
     uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
     constexpr bool kInt4 = FMT == kINT4;
-    constexpr uint32_t kRec = kInt4 ? 96 : 512;   // shared record bytes per warp and block
+    constexpr uint32_t kRec = kInt4 ? 96 : 512;   // shared record bytes per row block and k-block
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int Wk = blockDim.x >> 5;
     const int r = lane >> 2, c = lane & 3;
-    const int Wk = 1 << a.wk_log2;
-    const int blk = warp >> a.wk_log2, kw = warp & (Wk - 1);
-    const int rows = a.rb * 16;                                // rows of the widest CTA
-    // this CTA's row blocks: an even share of the Nb blocks (counts differ
-    // by at most one, never above rb)
-    const int bs = (int)((long long)blockIdx.x * a.Nb / gridDim.x);
-    const int be = (int)((long long)(blockIdx.x + 1) * a.Nb / gridDim.x);
+    constexpr int rows = RB * 16;
+    // this CTA's row blocks: an even share of the Nb blocks (at most RB)
+    const int bs = a.wide ? (int)((long long)blockIdx.x * a.Nb / gridDim.x)
+                          : (int)(blockIdx.x * (unsigned)a.Nb / gridDim.x);
+    const int be = a.wide ? (int)((long long)(blockIdx.x + 1) * a.Nb / gridDim.x)
+                          : (int)((blockIdx.x + 1) * (unsigned)a.Nb / gridDim.x);
+    const int nb = be - bs;
     const int n0 = bs * 16, n_end = min(a.N, be * 16);
-    const int b = bs + blk;                                    // this warp's row block
     const int mz = blockIdx.y * a.mrows;
     const int Mc = min(a.mrows, a.M - mz);
-    const int it0 = kw * a.ipw;
-    const int nrange = max(0, min(a.I, it0 + a.ipw) - it0);   // blocks of this K range
-    const int nit = b < be ? nrange : 0;                      // ... this warp computes
-    const uint32_t bar = sbase + 8 * warp, abar = sbase + 128 + 8 * kw;
-    const uint32_t wslice = sbase + a.w_off + (uint32_t)(warp * a.ipw) * 1024u;
-    const uint32_t rslice = sbase + a.r_off + (uint32_t)(warp * a.ipw) * kRec;
-    const size_t blk0 = (size_t)b * a.I + it0;
+    const int it0 = warp * a.ipw;
+    const int nit = max(0, min(a.I, it0 + a.ipw) - it0);   // this warp's k-blocks
+    const uint32_t rslice = sbase + a.rec_off + (uint32_t)(warp * RB * a.ipw) * kRec;
 
-    if (tid == 0) {
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mbar_init(sbase + 8 * w, 1);
-        for (int q = 0; q < Wk; ++q) mbar_init(sbase + 128 + 8 * q, 1);
-        fence_mbarrier_init();
-    }
+    Ring<RB> ring;
+    ring.slots = sbase + a.ring_off + (uint32_t)(warp * a.P) * a.slot_bytes;
+    ring.bar = sbase + 8u * (uint32_t)(warp * a.P);
+    ring.slot_bytes = a.slot_bytes;
+    ring.codes = a.codes + ((size_t)bs * a.I + it0) * 1024;
+    ring.row_stride = (size_t)a.I * 1024;
+    ring.asrc = a.A + (size_t)(mz + (lane >> 4)) * a.K + (size_t)it0 * 128 + 8 * (lane & 15);
+    ring.azero = a.A;
+    ring.lda2 = 2 * (size_t)a.K;
+    ring.krem = a.K - it0 * 128 - 8 * (lane & 15);
+    ring.adst = 1024u * RB + kAStride * (uint32_t)(lane >> 4) + 16u * (lane & 15);
+    ring.aunits = Mc > (lane >> 4) ? (Mc - (lane >> 4) + 1) >> 1 : 0;
+    ring.nb = nb;
+    ring.nit = nit;
+    ring.P = a.P;
+    ring.lane = lane;
+    const int npro = min(a.P, nit);
+
+    // with the inputs declared ready nothing waits on the preceding kernel
+    // before the stores, so the next call may be scheduled at once
+    if (a.inputs_ready) grid_dependents_launch();
+    if (lane < npro) mbar_init(ring.bar + 8 * lane, 32);
+    fence_mbarrier_init();
     __syncthreads();
 
-    // ---- 1. this warp's code blocks (and int4 record blocks), one copy each
-    if (lane == 0) {
-        mbar_arrive_expect_tx(bar, (uint32_t)nit * (1024u + (kInt4 ? 96u : 0u)));
-        if (nit > 0) {
-            bulk_copy_g2s(wslice, a.codes + blk0 * 1024, (uint32_t)nit * 1024u, bar);
-            if constexpr (kInt4) bulk_copy_g2s(rslice, a.recs + blk0 * 96, (uint32_t)nit * 96u, bar);
+    // ---- 1. records (int4: copied ahead of step 0's arrival, so that its
+    // barrier covers them) and the code blocks of the first P steps
+    if (nit > 0) {
+        if constexpr (kInt4) {
+            for (int q = 0; q < nb; ++q)
+                for (int u = lane; u < nit * 6; u += 32)
+                    cp_async16(rslice + (uint32_t)(q * a.ipw) * 96u + 16u * u,
+                               a.recs + ((size_t)(bs + q) * a.I + it0) * 96 + 16 * u);
         }
+        for (int t = 0; t < npro; ++t) ring.issue_codes(t, t);
     }
 
-    // ---- 2. fp4: decode multipliers into the lane order of the loop; zero
-    // the activation tail of a partial last block (its codes are 0, and
-    // 0 x garbage could be NaN)
+    // ---- 2. fp4: decode multipliers into the lane order of the loop
     bool two = false;
     if constexpr (!kInt4) {
         uint8_t* s8 = sgen + (rslice - sbase);
-        if constexpr (FMT == kNVFP4) {
-            // record block: row rho's 8 bytes at 8 rho; lane = (rho, half of
-            // the groups); group g feeds word j = g >> 1 of the lanes with
-            // (c >> 1) == (g & 1)
-            const int rho = lane >> 1, g0 = 4 * (lane & 1);
-            for (int t = 0; t < nit; ++t) {
-                const uint32_t raw = ldg_u32(a.recs + (blk0 + t) * 128 + 4 * lane);
-                const uint32_t f01 = e4m3x2_to_f16x2(raw & 0xFFFFu), f23 = e4m3x2_to_f16x2(raw >> 16);
-                const uint32_t hv[4] = {f01 & 0xFFFFu, f01 >> 16, f23 & 0xFFFFu, f23 >> 16};
+        for (int q = 0; q < nb; ++q) {
+            const size_t blk0 = (size_t)(bs + q) * a.I + it0;
+            uint8_t* sq = s8 + (size_t)q * a.ipw * 512;
+            if constexpr (FMT == kNVFP4) {
+                // record block: row rho's 8 bytes at 8 rho; lane = (rho, half
+                // of the groups); group g feeds word j = g >> 1 of the lanes
+                // with (c >> 1) == (g & 1)
+                const int rho = lane >> 1, g0 = 4 * (lane & 1);
+                for (int t = 0; t < nit; ++t) {
+                    const uint32_t raw = ldg_u32(a.recs + (blk0 + t) * 128 + 4 * lane);
+                    const uint32_t f01 = e4m3x2_to_f16x2(raw & 0xFFFFu), f23 = e4m3x2_to_f16x2(raw >> 16);
+                    const uint32_t hv[4] = {f01 & 0xFFFFu, f01 >> 16, f23 & 0xFFFFu, f23 >> 16};
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int g = g0 + q;
-                    const uint32_t off = t * 512 + (((rho & 7) * 2 + (g & 1)) * 32) + (rho >> 3) * 16 + (g >> 1) * 4;
-                    *reinterpret_cast<uint32_t*>(s8 + off) = splat16(nvfp4_mul_from_f16(hv[q]));
+                    for (int g4 = 0; g4 < 4; ++g4) {
+                        const int g = g0 + g4;
+                        const uint32_t off =
+                            t * 512 + (((rho & 7) * 2 + (g & 1)) * 32) + (rho >> 3) * 16 + (g >> 1) * 4;
+                        *reinterpret_cast<uint32_t*>(sq + off) = splat16(nvfp4_mul_from_f16(hv[g4]));
+                    }
+                }
+            } else {
+                // record block: row rho's 4 bytes at 4 rho, group g = word j
+                const int rho = lane & 15;
+                for (int t = lane >> 4; t < nit; t += 2) {
+                    const uint32_t raw = ldg_u32(a.recs + (blk0 + t) * 64 + 4 * rho);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const GroupKey k = key_mxfp4((raw >> (8 * g)) & 0xFFu);
+                        two |= k.two;
+                        const uint32_t off = t * 512 + (rho & 7) * 32 + (rho >> 3) * 16 + g * 4;
+                        *reinterpret_cast<uint32_t*>(sq + off) = k.mul;
+                        *reinterpret_cast<uint32_t*>(sq + off + 256) = k.mul2;
+                    }
                 }
             }
-        } else {
-            // record block: row rho's 4 bytes at 4 rho, group g = word j
-            const int rho = lane & 15;
-            for (int t = lane >> 4; t < nit; t += 2) {
-                const uint32_t raw = ldg_u32(a.recs + (blk0 + t) * 64 + 4 * rho);
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const GroupKey k = key_mxfp4((raw >> (8 * g)) & 0xFFu);
-                    two |= k.two;
-                    const uint32_t off = t * 512 + (rho & 7) * 32 + (rho >> 3) * 16 + g * 4;
-                    *reinterpret_cast<uint32_t*>(s8 + off) = k.mul;
-                    *reinterpret_cast<uint32_t*>(s8 + off + 256) = k.mul2;
-                }
-            }
-        }
-        if (nit > 0 && (it0 + nit) * 128 > a.K) {
-            const int t0 = (a.K - it0 * 128) * 2, t1 = nit * 256;   // bytes of the range
-            for (int m = 0; m < Mc; ++m)
-                for (int o = t0 + 16 * lane; o < t1; o += 512)
-                    sts128_zero(sbase + a.a_off + (uint32_t)m * a.SA + (uint32_t)it0 * 256 + o);
         }
         two = __any_sync(0xffffffffu, two);
+        __syncwarp();   // the lanes read multipliers other lanes wrote
     }
 
-    // the next kernel on the stream may start.  C is written only after the
+    // ---- 3. the next kernel may start.  C is written only after the
     // preceding kernel has finished; A is read after it too, unless the
     // caller declared it complete already (inputs_ready)
     grid_dependents_launch();
     if (!a.inputs_ready) grid_dependency_wait();
+    for (int t = 0; t < npro; ++t) ring.issue_acts(t, t);
 
-    // ---- 3. activations of this K range: the range's first warp copies them
-    if (blk == 0) {
-        const int kb = it0 * 128, ke = min(a.K, (it0 + nrange) * 128);
-        const uint32_t bytes = ke > kb ? (uint32_t)(ke - kb) * 2u : 0u;
-        if (lane == 0) mbar_arrive_expect_tx(abar, bytes * (uint32_t)Mc);
-        __syncwarp();
-        if (lane < Mc && bytes > 0)
-            bulk_copy_g2s(sbase + a.a_off + (uint32_t)lane * a.SA + (uint32_t)it0 * 256,
-                          a.A + (size_t)(mz + lane) * a.K + kb, bytes, abar);
-    }
-
-    // ---- 4. wait for this warp's codes and the range's activations --------
+    // ---- 4. the range, step by step as the slots land ----------------------
     constexpr int MP = NT * 8;
-    float acc[NT][4];
+    float acc[RB][NT][4];
 #pragma unroll
-    for (int t = 0; t < NT; ++t)
+    for (int q = 0; q < RB; ++q)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[t][e] = 0.f;
-    bool ok = mbar_wait_timeout(bar, 0, kWaitNs);
-    ok = mbar_wait_timeout(abar, 0, kWaitNs) && ok;
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[q][t][e] = 0.f;
+    bool ok = true;
+    if (nit > 0) {
+        uint32_t dummy = 0;
+        ok = ring.wait(0, 0u, dummy);   // step 0 (and the int4 records)
+        if (!ok) ring.drain(1, npro);
+    }
     if constexpr (kInt4) {
-        // a zero point above 128 anywhere in the slice: second subtrahends
+        // a zero point above 128 anywhere in the range: second subtrahends
         bool t2 = false;
         if (ok)
-            for (int q = lane; q < nit * 16; q += 32) t2 |= lds16(rslice + (q >> 4) * 96 + 64 + 2 * (q & 15)) != 0;
+            for (int q = 0; q < nb; ++q)
+                for (int u = lane; u < nit * 16; u += 32)
+                    t2 |= lds16(rslice + (uint32_t)(q * a.ipw + (u >> 4)) * 96u + 64u + 2u * (u & 15)) != 0;
         two = __any_sync(0xffffffffu, t2);
     }
     if (ok && nit > 0) {
-        // activation rows past Mc are not staged: those lanes read row 0 or 1
-        // (keeping the row parity of a staged neighbour)
-        uint32_t ap[NT];
+        // activation rows past Mc are not copied: those lanes read row 0 or 1
+        // (keeping the row parity of a copied neighbour); their outputs are
+        // never stored
+        uint32_t aoff[NT];
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             const int m = t * 8 + r;
             const int ms = m < Mc ? m : (Mc > 1 ? (m & 1) : 0);
-            ap[t] = sbase + a.a_off + (uint32_t)ms * a.SA + (uint32_t)(it0 * 256 + c * 16);
+            aoff[t] = 1024u * RB + kAStride * (uint32_t)ms + 16u * c;
         }
         const uint32_t lane_w = 32u * r + 16u * ((c >> 1) ^ ((r >> 2) & 1)) + 8u * (c & 1);
-        uint32_t wp = wslice + lane_w;
-        // the shared loads below must not move above the barrier waits
-        asm volatile("" : "+r"(wp)::"memory");
-#pragma unroll
-        for (int t = 0; t < NT; ++t) asm volatile("" : "+r"(ap[t])::"memory");
-        if constexpr (kInt4) {
-            const uint32_t rp = rslice + 8u * r, rq = rslice + 64u + 4u * r;
-            if (two) loop_int4<NT, true>(wp, rp, rq, ap, nit, acc);
-            else loop_int4<NT, false>(wp, rp, rq, ap, nit, acc);
-        } else {
-            const uint32_t rp = rslice + (FMT == kNVFP4 ? (2u * r + (c >> 1)) * 32u : 32u * r);
-            if (two) loop_fp4<NT, true>(wp, rp, ap, nit, acc);
-            else loop_fp4<NT, false>(wp, rp, ap, nit, acc);
-        }
+        const uint32_t rlane = kInt4 ? (uint32_t)r : (FMT == kNVFP4 ? (2u * r + (c >> 1)) * 32u : 32u * r);
+        ok = two ? run_range<FMT, NT, RB, true>(ring, lane_w, aoff, rslice, rlane, a.ipw, acc)
+                 : run_range<FMT, NT, RB, false>(ring, lane_w, aoff, rslice, rlane, a.ipw, acc);
     }
     if (!ok && lane == 0) record_pre_timeout();
     if (a.inputs_ready) grid_dependency_wait();   // completion order: stores after the predecessor's
-    if (__syncthreads_or(!ok)) return;   // a copy never landed: store nothing
+    if (__syncthreads_or(!ok)) return;           // a copy never landed: store nothing
 
     // ---- 5. partial sums -> shared memory, fixed-order reduction, store ----
     const int ld = rows + 4;
-    float* red = reinterpret_cast<float*>(sgen + a.red_off);
-    {
-        const int y = blk * 16 + r;
+    float* red = reinterpret_cast<float*>(sgen + a.ring_off);
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            const int m = t * 8 + 2 * c;
-            float* p = red + ((size_t)kw * MP + m) * ld + y;
-            p[0] = acc[t][0];
-            p[ld] = acc[t][1];
-            p[8] = acc[t][2];
-            p[ld + 8] = acc[t][3];
+    for (int q = 0; q < RB; ++q) {
+        if (q < nb) {
+            const int y = q * 16 + r;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const int m = t * 8 + 2 * c;
+                float* p = red + ((size_t)warp * MP + m) * ld + y;
+                p[0] = acc[q][t][0];
+                p[ld] = acc[q][t][1];
+                p[8] = acc[q][t][2];
+                p[ld + 8] = acc[q][t][3];
+            }
         }
     }
     __syncthreads();
     const bool gated = EPI && a.epi.gated;
-    const int outs = gated ? rows >> 1 : rows;   // a power of two
+    constexpr int outs_full = rows;
+    const int outs = gated ? outs_full >> 1 : outs_full;   // a power of two
     const int outs_log2 = 31 - __clz(outs);
     for (int i = tid; i < Mc * outs; i += blockDim.x) {
         const int m = i >> outs_log2, o = i & (outs - 1);
@@ -364,45 +525,46 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_pre_kernel(const Pr
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+constexpr int kMaxK = 16384;
+constexpr size_t kMaxSmem = 227 * 1024;
+
 struct Plan {
-    int rb = 0, wk_log2 = 0, threads = 0, ipw = 0;
+    int RB = 0, Wk = 0, P = 0, ipw = 0, grid = 0;
     size_t smem = 0;
-    uint32_t SA = 0, w_off = 0, a_off = 0, r_off = 0, red_off = 0;
+    uint32_t slot_bytes = 0, ring_off = 0, rec_off = 0;
 };
 
 using KernFn = void (*)(PreArgs);
 
-template <int FMT, int NT>
+template <int FMT, int NT, int RB>
 KernFn kernel_for(bool epi) {
-    return epi ? gemv_pre_kernel<FMT, NT, true> : gemv_pre_kernel<FMT, NT, false>;
+    return epi ? gemv_pre_kernel<FMT, NT, true, RB> : gemv_pre_kernel<FMT, NT, false, RB>;
+}
+template <int FMT, int NT>
+KernFn kernel_rb(int RB, bool epi) {
+    return RB == 1 ? kernel_for<FMT, NT, 1>(epi) : RB == 2 ? kernel_for<FMT, NT, 2>(epi) : kernel_for<FMT, NT, 4>(epi);
+}
+KernFn select_kernel(int fmt, int NT, int RB, bool epi) {
+    if (fmt == kNVFP4) return NT == 1 ? kernel_rb<kNVFP4, 1>(RB, epi) : kernel_rb<kNVFP4, 2>(RB, epi);
+    if (fmt == kMXFP4) return NT == 1 ? kernel_rb<kMXFP4, 1>(RB, epi) : kernel_rb<kMXFP4, 2>(RB, epi);
+    return NT == 1 ? kernel_rb<kINT4, 1>(RB, epi) : kernel_rb<kINT4, 2>(RB, epi);
 }
 
-KernFn select_kernel(int fmt, int NT, bool epi) {
-    if (fmt == kNVFP4) return NT == 1 ? kernel_for<kNVFP4, 1>(epi) : kernel_for<kNVFP4, 2>(epi);
-    if (fmt == kMXFP4) return NT == 1 ? kernel_for<kMXFP4, 1>(epi) : kernel_for<kMXFP4, 2>(epi);
-    return NT == 1 ? kernel_for<kINT4, 1>(epi) : kernel_for<kINT4, 2>(epi);
-}
+uint32_t round128(size_t x) { return (uint32_t)((x + 127) & ~(size_t)127); }
 
-constexpr size_t kMaxSmem = 227 * 1024;
-
-Plan layout(int rb, int wk_log2, int Mc, int I, int fmt, int MP) {
+// Shared memory of a CTA shape (section comment at the top of the file).
+Plan layout(int RB, int Wk, int P, int Mc, int I, int fmt, int MP) {
     Plan p;
-    p.rb = rb;
-    p.wk_log2 = wk_log2;
-    p.threads = (rb << wk_log2) * 32;
-    p.ipw = (I + (1 << wk_log2) - 1) >> wk_log2;
-    const size_t rows = (size_t)rb * 16, warps = (size_t)rb << wk_log2;
-    p.w_off = kBarBytes;
-    size_t off = p.w_off + warps * p.ipw * 1024;
-    p.a_off = (uint32_t)off;
-    p.SA = (uint32_t)I * 256 + 64;   // 64 (mod 128): row parities in opposite bank halves
-    off += (size_t)Mc * p.SA;
-    p.r_off = (uint32_t)off;
-    off += warps * p.ipw * (fmt == kINT4 ? 96 : 512);
-    p.red_off = kBarBytes;           // aliases W, A and R once every warp is done
-    const size_t red = ((size_t)1 << wk_log2) * MP * (rows + 4) * sizeof(float);
-    if (p.red_off + red > off) off = p.red_off + red;
-    p.smem = off + 128;              // base alignment slack
+    p.RB = RB;
+    p.Wk = Wk;
+    p.ipw = (I + Wk - 1) / Wk;
+    p.P = P < p.ipw ? P : p.ipw;
+    p.ring_off = round128((size_t)8 * Wk * p.P);
+    p.slot_bytes = round128((size_t)1024 * RB + (size_t)kAStride * Mc);
+    p.rec_off = p.ring_off + (uint32_t)(Wk * p.P) * p.slot_bytes;
+    const size_t end = p.rec_off + (size_t)Wk * RB * p.ipw * (fmt == kINT4 ? 96 : 512);
+    const size_t red = p.ring_off + (size_t)Wk * MP * (RB * 16 + 4) * sizeof(float);
+    p.smem = (end > red ? end : red) + 128;   // + base alignment slack
     return p;
 }
 
@@ -411,55 +573,107 @@ int env_int(const char* name, int dflt) {
     return e ? atoi(e) : dflt;
 }
 
-// The CTA shape and grid.  A CTA takes an even share of the row blocks
-// (rb = the largest share) x all of K, split over Wk warps.  Cost, in SM
-// issue cycles of the busiest SM: its block iterations / 4 schedulers, the
-// activation bytes it receives, one warp's run and a latency round per extra
-// wave.  Chained launches (pdl) stream the next call's weights while this
-// one computes only if its CTAs fit beside this kernel's own; and a grid
-// smaller than the SM count lets the next call put two CTAs on an SM this
-// call left idle, which then runs twice the work -- so a grid of exactly one
-// CTA per SM is preferred there.
-bool choose_plan(KernFn kern, int fmt, int NT, int Mc, int mchunks, int Nb, int I, int sms, bool pdl, Plan& best,
-                 int& grid) {
+// Kernels take up to 227 KB of dynamic shared memory (set once per device
+// and kernel, before any occupancy query or launch).
+bool allow_smem(int dev, KernFn kern) {
+    static std::mutex mu;
+    static std::map<std::pair<int, KernFn>, bool> done;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[{dev, kern}]) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem) != cudaSuccess)
+        return false;
+    done[{dev, kern}] = true;
+    return true;
+}
+
+// The CTA shape: RB row blocks per CTA (grid = ceil(Nb / RB)), Wk warps (K
+// ranges) per CTA, P ring slots per warp.  Two regimes:
+//   inputs ready  the call overlaps the calls before and after it end to
+//                 end, so what counts is how many calls' CTAs share an SM
+//                 (small CTAs, a ring of 3) and the activation bytes each SM
+//                 copies (all of K per CTA);
+//   otherwise     the call's product can only start once its predecessor
+//                 has finished, so the whole range is requested at once
+//                 (P = the range) while that one runs, and the product after
+//                 the wait needs enough warps to keep the SM busy; a chained
+//                 call only streams early if its CTAs fit beside the
+//                 previous call's.
+// Overlapped and plain launches share a plan, so that flag never changes the
+// result's bits (the ready plan may split K differently: a rounding-level
+// difference, within the gate).  Costs are SM cycles of one call.
+// WQ_RING_RB / WQ_RING_WK (log2 of Wk) / WQ_RING_P force a shape (tests,
+// sweeps).
+bool choose_plan(int dev, int fmt, int NT, bool epi, int Mc, int mchunks, int Nb, int I, int K, int sms, bool ready,
+                 Plan& best) {
     const int MP = NT * 8;
-    const int force_rb = env_int("WQ_GEMV_RB", 0), force_wk = env_int("WQ_GEMV_TMA_WK", -1);
-    const double c_it = NT == 1 ? 130.0 : 150.0;
+    const int force_rb = env_int("WQ_RING_RB", 0), force_wk = env_int("WQ_RING_WK", -1);
+    const int force_p = env_int("WQ_RING_P", 0);
+    const double c_it = NT == 1 ? 140.0 : 170.0;   // issue cycles of one warp per 16 x 128 block
+    if (ready && !force_rb && force_wk < 0 && force_p <= 0) {
+        // Measured on GB300 (chained int4 calls, N = 8192, K = 3072, M = 1, 4
+        // and 16; every (RB, Wk, P) in {1,2,4} x {1,2,4,8} x {2,3,4} tried):
+        // two-slot rings, two row blocks per CTA and ~512 warps per call are
+        // best or within 3 % of it at every M -- small CTAs of many calls
+        // keep the SMs' decode and the HBM stream busy together.  Take that
+        // shape when it fits (one row block per CTA when two would leave
+        // fewer CTAs than SMs), else fall through to the cost model.
+        const int RB = Nb >= 2 * sms ? 2 : 1;
+        const int G = (Nb + RB - 1) / RB;
+        const double want = 512.0 / ((double)G * mchunks);
+        int Wk = 1;
+        while (Wk < (1 << kMaxWkLog2) && Wk < want && 2 * Wk <= I) Wk *= 2;
+        const KernFn kern = select_kernel(fmt, NT, RB, epi);
+        if (!allow_smem(dev, kern)) return false;
+        const Plan p = layout(RB, Wk, 2, Mc, I, fmt, MP);
+        int occ = 0;
+        if (p.smem <= kMaxSmem &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Wk * 32, p.smem) == cudaSuccess && occ >= 1) {
+            best = p;
+            best.grid = G;
+            return true;
+        }
+    }
     double best_cost = -1.0;
-    // (grid, blocks per CTA at most): fixed CTA widths, and one or two CTAs
-    // per SM with the blocks shared out evenly
-    int cg[6], crb[6], nc = 0;
-    for (int rb = 1; rb <= 8; rb *= 2, ++nc) {
-        cg[nc] = (Nb + rb - 1) / rb;
-        crb[nc] = rb;
-    }
-    for (int q = 1; q <= 2; ++q, ++nc) {
-        cg[nc] = Nb < q * sms ? Nb : q * sms;
-        crb[nc] = (Nb + cg[nc] - 1) / cg[nc];
-    }
-    for (int ci = 0; ci < nc; ++ci) {
-        const int G = cg[ci], rb = crb[ci];
-        if (rb > 8 || (force_rb && rb != force_rb)) continue;
+    for (int RB = 1; RB <= 4; RB *= 2) {
+        if (force_rb && RB != force_rb) continue;
+        const KernFn kern = select_kernel(fmt, NT, RB, epi);
+        if (!allow_smem(dev, kern)) return false;
+        const int G = (Nb + RB - 1) / RB;
         for (int wk = 0; wk <= kMaxWkLog2; ++wk) {
+            const int Wk = 1 << wk;
             if (force_wk >= 0 && wk != force_wk) continue;
-            if ((rb << wk) * 32 > 512) continue;
-            if (force_wk < 0 && wk > 0 && (1 << wk) > I) continue;
-            const Plan p = layout(rb, wk, Mc, I, fmt, MP);
-            if (p.ipw > kMaxIpw || p.smem > kMaxSmem) continue;
+            if (force_wk < 0 && wk > 0 && Wk > I) continue;
+            const int ipw = (I + Wk - 1) / Wk;
+            int P = force_p > 0 ? force_p : (ready ? 3 : ipw);
+            Plan p = layout(RB, Wk, P, Mc, I, fmt, MP);
+            // not ready: the deepest ring that fits (steps beyond it stream
+            // after the dependency wait)
+            while (p.smem > kMaxSmem && !ready && force_p <= 0 && P > 2) p = layout(RB, Wk, --P, Mc, I, fmt, MP);
+            if (p.smem > kMaxSmem) continue;
             int occ = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, p.threads, p.smem) != cudaSuccess || occ < 1)
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Wk * 32, p.smem) != cudaSuccess || occ < 1)
                 continue;
-            const long long ctas = (long long)G * mchunks;
-            long long per_sm = (ctas + sms - 1) / sms;
-            if (pdl && occ >= 2 && ctas < sms) per_sm = 2;   // the next call doubles up on idle SMs
-            const long long waves = (ctas + (long long)sms * occ - 1) / ((long long)sms * occ);
-            double cost = per_sm * rb * I * c_it / 4.0 + per_sm * (double)Mc * I * 128 * 2 / 64.0 + p.ipw * c_it +
-                          (waves - 1) * 2500.0;
-            if (pdl && occ < 2 * ((ctas + sms - 1) / sms)) cost += 4000.0;
+            const double ctas = (double)G * mchunks, per_sm = ctas / sms;
+            const double act = per_sm * (double)Mc * K * 2 / 64.0;
+            double cost;
+            if (ready) {
+                cost = act + per_sm * 800.0 + (double)RB * p.ipw * c_it * 0.5;
+                const double depth = occ / per_sm;   // calls whose CTAs fit on an SM together
+                if (depth < 3.0) cost += (3.0 - depth) * 1500.0;
+            } else {
+                const double busiest = ceil(per_sm);
+                const double loop_sm = busiest * RB * I * c_it / 4.0;                   // issue-bound
+                const double loop_warp = (double)RB * p.ipw * c_it * 3.0;               // latency-bound
+                cost = act + busiest * 800.0 + (loop_sm > loop_warp ? loop_sm : loop_warp);
+                const double waves = ceil(ctas / ((double)sms * occ));
+                cost += (waves - 1.0) * 2500.0;
+                if (occ < 2.0 * busiest) cost += 4000.0;   // no room for the next call's CTAs
+                cost += (double)(p.ipw - p.P) / p.ipw * 3000.0;   // steps fetched after the wait
+            }
             if (best_cost < 0 || cost < best_cost) {
                 best_cost = cost;
                 best = p;
-                grid = G;
+                best.grid = G;
             }
         }
     }
@@ -467,71 +681,64 @@ bool choose_plan(KernFn kern, int fmt, int NT, int Mc, int mchunks, int Nb, int 
 }
 
 struct PlanKey {
-    int dev, fmt, NT, Mc, mchunks, N, K, pdl, epi;
+    int dev, fmt, NT, Mc, mchunks, N, K, epi, ready;
     bool operator<(const PlanKey& o) const {
-        return std::tie(dev, fmt, NT, Mc, mchunks, N, K, pdl, epi) <
-               std::tie(o.dev, o.fmt, o.NT, o.Mc, o.mchunks, o.N, o.K, o.pdl, o.epi);
+        return std::tie(dev, fmt, NT, Mc, mchunks, N, K, epi, ready) <
+               std::tie(o.dev, o.fmt, o.NT, o.Mc, o.mchunks, o.N, o.K, o.epi, o.ready);
     }
 };
 
 }  // namespace
 
+// Calls that declare their inputs ready run this file's ring kernel;
+// dependent and plain calls the staged kernel (wq_gemv_staged.cu), which
+// requests a CTA's whole slice before its dependency wait.
+// WQ_GEMV_PRE_KERNEL=ring|staged forces one of them (tests).
 int launch_gemv_prepacked(const void* A, const void* prepacked, void* C, int M, int N, int K, int fmt,
                           bool out_f32, bool pdl, bool inputs_ready, const Epilogue& epi, cudaStream_t stream) {
+    const char* force = getenv("WQ_GEMV_PRE_KERNEL");
+    const bool ring = force ? strcmp(force, "staged") != 0 : inputs_ready;
+    if (!ring) return launch_gemv_staged(A, prepacked, C, M, N, K, fmt, out_f32, pdl, inputs_ready, epi, stream);
     if (inputs_ready) pdl = true;
     if (M == 0 || N == 0) return WQ_OK;
-    if (K <= 0 || K > kMaxIpw * (1 << kMaxWkLog2) * 128) return WQ_ERR_UNSUPPORTED;
+    if (K <= 0 || K > kMaxK) return WQ_ERR_UNSUPPORTED;
     const int I = (K + 127) / 128, Nb = (N + 15) / 16;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const bool has_epi = epi.bias || epi.residual || epi.gated;
 
-    // 16 activation rows per CTA (two mma tiles) when they fit beside the
-    // weights, else 8, 4, 2 or 1 (one tile; long rows leave room for few)
+    // 16 activation rows per CTA (two MMA tiles) above 8 rows, else one tile
+    const int mrows = M > 8 ? 16 : 8;
+    const int NT = mrows == 16 ? 2 : 1;
+    const int Mc = M < mrows ? M : mrows;
+    const int mchunks = (M + mrows - 1) / mrows;
+    if (mchunks > 65535) return WQ_ERR_UNSUPPORTED;
     Plan plan;
-    KernFn kern = nullptr;
-    int mrows = 0, grid = 0;
+    bool fits;
     {
         static std::mutex mu;
-        static std::map<PlanKey, std::tuple<Plan, int, bool>> cache;   // shape -> (plan, grid, fits)
-        static std::map<std::pair<int, KernFn>, bool> attr_set;
-        const bool overridden = getenv("WQ_GEMV_RB") || getenv("WQ_GEMV_TMA_WK");
+        static std::map<PlanKey, std::pair<Plan, bool>> cache;   // shape -> (plan, fits)
+        const bool overridden = getenv("WQ_RING_RB") || getenv("WQ_RING_WK") || getenv("WQ_RING_P");
         std::lock_guard<std::mutex> lock(mu);
-        for (int mr = (M > 8 ? 16 : 8); mr >= 1 && !kern; mr = mr == 16 ? 8 : mr / 2) {
-            const int NT = mr == 16 ? 2 : 1;
-            const int Mc = M < mr ? M : mr;
-            const int mchunks = (M + mr - 1) / mr;
-            if (mchunks > 65535) return WQ_ERR_UNSUPPORTED;
-            KernFn kf = select_kernel(fmt, NT, has_epi);
-            if (!attr_set[{dev, kf}]) {
-                if (cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem) !=
-                    cudaSuccess)
-                    return WQ_ERR_CUDA;
-                attr_set[{dev, kf}] = true;
-            }
-            const PlanKey key{dev, fmt, NT, Mc, mchunks, N, K, pdl ? 1 : 0, has_epi ? 1 : 0};
-            auto it = overridden ? cache.end() : cache.find(key);
-            bool fits;
-            if (it != cache.end()) {
-                std::tie(plan, grid, fits) = it->second;
-            } else {
-                fits = choose_plan(kf, fmt, NT, Mc, mchunks, Nb, I, sms, pdl, plan, grid);
-                if (!overridden) cache[key] = std::make_tuple(plan, grid, fits);
-            }
-            if (fits) {
-                kern = kf;
-                mrows = mr;
-            }
+        const PlanKey key{dev, fmt, NT, Mc, mchunks, N, K, has_epi ? 1 : 0, inputs_ready ? 1 : 0};
+        auto it = overridden ? cache.end() : cache.find(key);
+        if (it != cache.end()) {
+            std::tie(plan, fits) = it->second;
+        } else {
+            fits = choose_plan(dev, fmt, NT, has_epi, Mc, mchunks, Nb, I, K, sms, inputs_ready, plan);
+            if (!overridden) cache[key] = std::make_pair(plan, fits);
         }
     }
-    if (!kern) {
+    if (!fits) {
         if (debug_on()) fprintf(stderr, "wq: prepacked GEMV: no CTA shape fits M=%d N=%d K=%d\n", M, N, K);
         return WQ_ERR_UNSUPPORTED;
     }
+    KernFn kern = select_kernel(fmt, NT, plan.RB, has_epi);
+    if (!allow_smem(dev, kern)) return WQ_ERR_CUDA;
     if (debug_on())
-        fprintf(stderr, "wq: prepacked GEMV M=%d N=%d K=%d: rows/CTA=%d grid=%d rb=%d wk=%d threads=%d smem=%zu\n", M,
-                N, K, mrows, grid, plan.rb, 1 << plan.wk_log2, plan.threads, plan.smem);
+        fprintf(stderr, "wq: prepacked GEMV M=%d N=%d K=%d: rows/CTA=%d grid=%d RB=%d Wk=%d P=%d threads=%d smem=%zu\n",
+                M, N, K, mrows, plan.grid, plan.RB, plan.Wk, plan.P, plan.Wk * 32, plan.smem);
 
     const uint8_t* base = static_cast<const uint8_t*>(prepacked);
     PreArgs args;
@@ -546,20 +753,18 @@ int launch_gemv_prepacked(const void* A, const void* prepacked, void* C, int M, 
     args.Nb = Nb;
     args.out_f32 = out_f32 ? 1 : 0;
     args.mrows = mrows;
-    args.rb = plan.rb;
-    args.wk_log2 = plan.wk_log2;
     args.ipw = plan.ipw;
-    args.SA = plan.SA;
-    args.w_off = plan.w_off;
-    args.a_off = plan.a_off;
-    args.r_off = plan.r_off;
-    args.red_off = plan.red_off;
+    args.P = plan.P;
+    args.slot_bytes = plan.slot_bytes;
+    args.ring_off = plan.ring_off;
+    args.rec_off = plan.rec_off;
+    args.wide = (unsigned long long)(plan.grid + 1) * (unsigned long long)Nb >= (1ull << 32) ? 1 : 0;
     args.inputs_ready = inputs_ready ? 1 : 0;
     args.epi = epi;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid, (M + mrows - 1) / mrows, 1);
-    cfg.blockDim = dim3(plan.threads, 1, 1);
+    cfg.gridDim = dim3(plan.grid, mchunks, 1);
+    cfg.blockDim = dim3(plan.Wk * 32, 1, 1);
     cfg.dynamicSmemBytes = plan.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

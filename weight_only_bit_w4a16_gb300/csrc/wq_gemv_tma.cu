@@ -86,6 +86,7 @@ struct TmaGemvArgs {
     uint32_t S;         // shared row stride of the packed weights (bytes)
     uint32_t SA;        // shared row stride of the activations (bytes)
     uint32_t w_off, a_off, r8_off, r4_off, bar_off, red_off;
+    int inputs_ready;   // A may be read before the preceding kernel completes
     Epilogue epi;
 };
 
@@ -311,9 +312,10 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_stream_kernel(const
     // the next kernel on the stream may start (programmatic dependent launch:
     // triggered once this CTA's own weight requests are out, so the next
     // call's stream follows this one's instead of competing with it); A is
-    // read, and C written, only after the preceding kernel has finished
+    // read, and C written, only after the preceding kernel has finished --
+    // A before it when the caller declared A complete already (inputs_ready)
     grid_dependents_launch();
-    grid_dependency_wait();
+    if (!a.inputs_ready) grid_dependency_wait();
 
     // ---- 4. activations of this K range, staged once by the rb warps that
     // share it (rows SA bytes apart, SA = 64 mod 128; units at a_pos) -------
@@ -382,6 +384,7 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_stream_kernel(const
             warp_loop<FMT, NT, MODE, false>(wp, 8 * a.S, rp, rq, ap, nit, acc);
     }
     if (!ok && lane == 0) record_gemv_timeout();
+    if (a.inputs_ready) grid_dependency_wait();   // completion order: stores after the predecessor's
     if (__syncthreads_or(!ok)) return;   // a copy never landed: store nothing
 
     // ---- 6. partial sums -> shared memory, fixed-order reduction, store ----
@@ -548,8 +551,9 @@ struct PlanKey {
 // this kernel: K = 0, K > 16384, or a CTA's activations + weights + records
 // above the shared-memory limit.
 int launch_gemv_tma(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C,
-                    int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, const Epilogue& epi,
-                    cudaStream_t stream) {
+                    int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, bool inputs_ready,
+                    const Epilogue& epi, cudaStream_t stream) {
+    if (inputs_ready) pdl = true;
     if (M == 0 || N == 0) return WQ_OK;
     if (K <= 0 || K > kMaxIpw * (1 << kMaxWkLog2) * kItK) return WQ_ERR_UNSUPPORTED;
     const int n_its = (K + kItK - 1) / kItK;
@@ -619,6 +623,7 @@ int launch_gemv_tma(const void* A, const uint8_t* packed, const void* scales, co
     args.r4_off = plan.r4_off;
     args.bar_off = plan.bar_off;
     args.red_off = plan.red_off;
+    args.inputs_ready = inputs_ready ? 1 : 0;
     args.epi = epi;
 
     cudaLaunchConfig_t cfg = {};

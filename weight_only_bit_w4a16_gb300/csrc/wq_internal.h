@@ -16,16 +16,19 @@ int launch_dequant(const uint8_t* packed, const void* scales, const uint8_t* zer
 
 // pdl: launch with programmatic dependent launch (the kernel streams its
 // weights before the preceding kernel on the stream has finished)
+// inputs_ready: A was complete before the chain of overlapped launches
+// began, so the kernel may read it at once and wait for its predecessor only
+// before storing C (implies pdl)
 int launch_gemv(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
-                void* C, int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, const Epilogue& epi,
-                cudaStream_t stream);
+                void* C, int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, bool inputs_ready,
+                const Epilogue& epi, cudaStream_t stream);
 
 // The streaming small-M kernel (all of a CTA's weights requested by TMA up
 // front).  Returns WQ_ERR_UNSUPPORTED (without launching) for shapes it does
 // not take; launch_gemv then uses the register-streaming kernels.
 int launch_gemv_tma(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
-                    void* C, int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, const Epilogue& epi,
-                    cudaStream_t stream);
+                    void* C, int M, int N, int K, int fmt, int group, bool out_f32, bool pdl, bool inputs_ready,
+                    const Epilogue& epi, cudaStream_t stream);
 
 // Returns WQ_ERR_UNSUPPORTED (without launching) for shapes the tensor-core
 // kernel does not take.  With a workspace of at least tc_workspace_bytes()
@@ -49,11 +52,11 @@ int launch_tc_prepacked(const void* A, const void* prepacked, void* C, int M, in
 size_t prepack_bytes(int N, int K, int fmt);
 int launch_prepack(const uint8_t* packed, const void* scales, const uint8_t* zeros, void* out, int N, int K,
                    int fmt, cudaStream_t stream);
-// inputs_ready: A was complete before the chain of overlapped launches began,
-// so the kernel reads it at once and waits for its predecessor only before
-// storing C (implies pdl)
 int launch_gemv_prepacked(const void* A, const void* prepacked, void* C, int M, int N, int K, int fmt,
                           bool out_f32, bool pdl, bool inputs_ready, const Epilogue& epi, cudaStream_t stream);
+// the staged small-M kernel on prepacked weights (dependent and plain calls)
+int launch_gemv_staged(const void* A, const void* prepacked, void* C, int M, int N, int K, int fmt, bool out_f32,
+                       bool pdl, bool inputs_ready, const Epilogue& epi, cudaStream_t stream);
 
 // The library's own stream-K scratch (a file-scope device array of the
 // tensor-core module) on the current device and its size; NULL if the
@@ -68,6 +71,7 @@ int launch_timeout_selftest(cudaStream_t stream);
 int read_and_clear_device_status();
 int read_and_clear_gemv_status();
 int read_and_clear_pre_status();
+int read_and_clear_staged_status();
 
 // WQ_DEBUG=1 in the environment prints why a call was refused.
 bool debug_on();

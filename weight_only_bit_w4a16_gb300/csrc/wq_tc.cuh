@@ -90,6 +90,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Wait with a wall-time bound and the suspend-time hint: a waiting warp
+// sleeps (up to ~200 ns, waking as soon as the phase completes) instead of
+// spinning, leaving the issue slots to the warps that have work.  Used by the
+// small-M kernel, whose waiting warps share the SM with other CTAs' loops.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait_hint(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait_hint(bar, parity)) return true;
+        if ((i & 15) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // Wait with a wall-time bound only (no abort check): used when a CTA unwinds
 // and must still see its own copies / MMAs complete before it exits.
 __device__ __forceinline__ bool mbar_wait_timeout(uint32_t bar, uint32_t parity, uint64_t limit_ns) {

@@ -71,6 +71,37 @@ BENCH_WORKLOADS = {
 }
 DEFAULT_STEPS = {"layer_sweep": (300, 10)}   # (steps, warm-up) when not given: one step is ~2 ms
 
+# launch modes of the small-M calls (include/wq.h); the tensor-core path
+# ignores both bits
+LAUNCH_FLAGS = {
+    "ready": lambda wq: wq.WQ_LAUNCH_INPUTS_READY,
+    "overlap": lambda wq: wq.WQ_LAUNCH_OVERLAP,
+    "plain": lambda wq: 0,
+}
+LAUNCH_DESC = {
+    "ready": "WQ_LAUNCH_INPUTS_READY (programmatic dependent launch; the activations were written before the "
+             "chain, so each call reads them at once and waits for its predecessor only before storing C)",
+    "overlap": "WQ_LAUNCH_OVERLAP (programmatic dependent launch; each call reads A after its predecessor "
+               "completes: a dependent chain)",
+    "plain": "plain launches",
+}
+SPIN_CYCLES = 100000   # ~50 us spin ahead of a start event (device clock cycles)
+
+
+def bench_config(workload: str, ws: int) -> dict:
+    """The workload a line measures: identical in both arms (how our arm
+    launches and lays out its weights is under the line's "setup")."""
+    w = BENCH_WORKLOADS[workload]
+    cfg = {"workload": workload, "format": w["fmt"], "group": w["group"], "M": list(w["Ms"]), "out": w["out"]}
+    if workload == "layer_sweep":
+        from weight_only_bit_w4a16_gb300 import synth
+        cfg["calls"] = {c: list(synth.LAYER_SHAPES[fam]) for c, fam in w["calls"]}
+        cfg["calls_per_step"] = len(w["Ms"]) * len(w["calls"])
+    else:
+        cfg.update(N=w["N"], K=w["K"], calls_per_step=len(w["Ms"]))
+    cfg["parallelism"] = f"replicas x{ws}"
+    return cfg
+
 KERNEL_SOURCES = {  # files whose content defines the dominant kernel of a workload (and layout)
     "decode_int4": ["wq_gemv_tma.cu", "wq_gemv.cuh", "wq_common.cuh"],
     "decode_int4:prepacked": ["wq_gemv_pre.cu", "wq_gemv.cuh", "wq_common.cuh"],
@@ -335,10 +366,14 @@ def run_ours(args):
     C_d = {M: torch.empty((M, N), dtype=odt, device=dev) for M in Ms}
     s = torch.cuda.Stream(dev)
 
-    # the weights are never written by the kernels of the step, so every call
-    # may overlap the previous one (WQ_LAUNCH_OVERLAP, programmatic dependent
-    # launch); the plain launch is timed as well and reported beside it
-    overlap = wq.WQ_LAUNCH_OVERLAP if not args.no_overlap else 0
+    # Launch mode of the timed calls.  The weights are never written by the
+    # kernels of the step and the activations are written before the step,
+    # so every call may declare its inputs ready (WQ_LAUNCH_INPUTS_READY:
+    # the calls overlap end to end and still complete in stream order);
+    # "overlap" times the dependent chain (WQ_LAUNCH_OVERLAP: A read after
+    # the preceding call completes), "plain" ordinary launches.  The modes
+    # not timed as the value are reported beside it.
+    overlap = LAUNCH_FLAGS[args.launch](wq)
 
     def call(M, slot, stream_handle, flags=None):
         fl = overlap if flags is None else flags
@@ -373,13 +408,18 @@ def run_ours(args):
             for j, M in enumerate(Ms):
                 call(M, j, s.cuda_stream)
     torch.cuda.synchronize()
-    g_full = capture(G, Ms)
+    g_full = capture(G, Ms) if args.steps >= G else None
     rem = args.steps % G
     g_rem = capture(rem, Ms) if rem else None
 
-    # warm-up (untimed): at least W steps
-    for _ in range(max(1, math.ceil(args.warmup / G))):
-        g_full.replay()
+    # warm-up (untimed): at least W steps, and every graph the timed region
+    # replays has been replayed before it (a graph's first replay uploads it)
+    warm = 0
+    while warm < max(1, args.warmup) or warm == 0:
+        for g_ in (g_full, g_rem):
+            if g_ is not None:
+                g_.replay()
+                warm += G if g_ is g_full else rem
     torch.cuda.synchronize()
 
     gpu_id = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else str(local)
@@ -390,6 +430,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     t0 = time.monotonic()
     with torch.cuda.stream(s):
+        # a short spin ahead of the start event: the graph launches are queued
+        # behind it, so host-side submission is not inside the timed window
+        torch.cuda._sleep(SPIN_CYCLES)
         ev0.record(s)
         for _ in range(args.steps // G):
             g_full.replay()
@@ -426,66 +469,82 @@ def run_ours(args):
                 "frac": achieved / peak, "traffic": profiled_traffic(traffic_key),
                 "algorithmic_flops_per_launch": algo, "peak_source": peaks["source"] + " bf16_tflops (burst)"}
 
-    # the same steps with plain launches (no overlap), not part of the value
-    g_plain = capture(G, Ms, flags=0)
-    g_plain.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(s):
-        e0.record(s)
-        for _ in range(max(1, args.steps // G)):
-            g_plain.replay()
-        e1.record(s)
-    torch.cuda.synchronize()
-    plain_ms_per_step = e0.elapsed_time(e1) / (max(1, args.steps // G) * G)
+    def replay_ms(g_, n_steps, reps):
+        """Milliseconds per step of `reps` replays of a warmed graph of
+        n_steps steps (spin kernel ahead of the start event)."""
+        g_.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            torch.cuda._sleep(SPIN_CYCLES)
+            e0.record(s)
+            for _ in range(reps):
+                g_.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (reps * n_steps)
+
+    def step_value(ms_step):
+        return ws * (per_step_w if w["bound"] == "hbm" else sum(metrics.call_flops(M, N, K) for M in Ms)) / \
+            (ms_step / 1e3) / (1e9 if w["bound"] == "hbm" else 1e12)
+
+    # the same steps in the other launch modes, not part of the value
+    other_modes = {}
+    for mode in LAUNCH_FLAGS:
+        if mode == args.launch:
+            continue
+        g_m = capture(G, Ms, flags=LAUNCH_FLAGS[mode](wq))
+        ms_m = replay_ms(g_m, G, max(1, min(args.steps, 2000) // G))
+        other_modes[mode] = {"ms_per_step": ms_m, "value": step_value(ms_m), "launch": LAUNCH_DESC[mode]}
+        del g_m
 
     # per-M launch time (separate graphs of one M; not part of the timed steps)
     per_m = {}
     if w["bound"] == "hbm" and len(Ms) > 1:
         for M in Ms:
-            gm = capture(R, (M,))
-            gm.replay()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            reps = max(1, 2000 // R)
-            with torch.cuda.stream(s):
-                e0.record(s)
-                for _ in range(reps):
-                    gm.replay()
-                e1.record(s)
-            torch.cuda.synchronize()
-            us = e0.elapsed_time(e1) * 1e3 / (reps * R)
-            cb = metrics.call_bytes(fmt, M, N, K, group, out)
-            per_m[str(M)] = {"us_per_call": us, "weight_GBps": wb / us / 1e3,
-                             "roofline_frac": cb / us / 1e3 / peaks["hbm_gbs"]}
+            entry = {}
+            for mode in ([args.launch] + [m for m in LAUNCH_FLAGS if m != args.launch and m != "plain"]):
+                gm = capture(R, (M,), flags=LAUNCH_FLAGS[mode](wq))
+                us = replay_ms(gm, R, max(1, 2000 // R)) * 1e3
+                del gm
+                cb = metrics.call_bytes(fmt, M, N, K, group, out)
+                d = {"us_per_call": us, "weight_GBps": wb / us / 1e3, "roofline_frac": cb / us / 1e3 / peaks["hbm_gbs"]}
+                if mode == args.launch:
+                    entry.update(d)
+                else:
+                    entry[mode] = d
+            per_m[str(M)] = entry
 
     e2e = run_e2e(args, w, A_by_M, weights, pool, dev, ws, pre_pool)
-    fused = fused_gate_up(w, dev, l2) if (w["bound"] == "hbm" and fmt == "int4" and not args.no_overlap) else None
+    fused = fused_gate_up(w, dev, l2) if (w["bound"] == "hbm" and fmt == "int4" and args.launch != "plain") else None
+    tensor_core = None
+    if args.workload == "decode_int4" and not args.no_tensor_core:
+        del pool, pre_pool
+        torch.cuda.empty_cache()
+        tensor_core = tensor_core_block(args, dev, gpu_id, peaks)
 
     result = {
         "metric": w["metric"], "value": value, "unit": w["unit"], "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "format": fmt, "group": group, "M": list(Ms), "N": N, "K": K,
-                   "out": out, "calls_per_step": len(Ms),
-                   "l2": f"inputs larger than L2: {R} weight sets of {wb / 1e6:.2f} MB rotated "
-                         f"({R * wb / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
-                   "timing": "CUDA graphs of the timed steps, CUDA events on the launching stream",
-                   "launch": "WQ_LAUNCH_OVERLAP (programmatic dependent launch)" if overlap else "plain",
-                   "layout": ("prepacked (wq_prepack, untimed build step)" if prepacked else
-                              "as given (packed, scales, zeros)"),
-                   "parallelism": f"replicas x{ws}"},
+        "config": bench_config(args.workload, ws),
+        "setup": {"l2": f"inputs larger than L2: {R} weight sets of {wb / 1e6:.2f} MB rotated "
+                        f"({R * wb / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
+                  "timing": "CUDA graphs of the timed steps (each replayed once before timing), CUDA events on "
+                            "the launching stream, a short spin kernel ahead of the start event",
+                  "launch": LAUNCH_DESC[args.launch],
+                  "layout": ("prepacked (wq_prepack, untimed build step)" if prepacked else
+                             "as given (packed, scales, zeros)")},
         "roofline": roof, "clocks": clocks, "gpu_launches": launches, "e2e": e2e,
-        "plain_launch": {"ms_per_step": plain_ms_per_step,
-                         "value": ws * (per_step_w if w["bound"] == "hbm" else
-                                        sum(metrics.call_flops(M, N, K) for M in Ms)) /
-                                  (plain_ms_per_step / 1e3) / (1e9 if w["bound"] == "hbm" else 1e12)},
+        "other_launch_modes": other_modes,
     }
     if per_m:
         result["per_m"] = per_m
     if fused:
         result["fused_gate_up"] = fused
+    if tensor_core:
+        result["tensor_core"] = tensor_core
     if rank == 0 and ws == 1:
         result["cpu_baseline"] = cpu_baseline(w, A_by_M, weights, budget_s=args.cpu_budget)
     if rank == 0:
@@ -571,6 +630,126 @@ def fused_gate_up(w, dev, l2):
         out[str(M)] = res
     return {"shape": f"gate + up {N} x {K} int4 g{group} each (fused: one {2 * N}-row call, SiLU-gated "
                      f"epilogue; unfused: two calls + torch silu and mul)", "per_m": out}
+
+
+# ---------------------------------------------------------------------------
+# the tensor-core configurations, timed in the default run
+# ---------------------------------------------------------------------------
+def tensor_core_block(args, dev, gpu_id, peaks):
+    """The large-M configurations beside the decode line: the MXFP4 prefill
+    (2048 x 3072 x 3072) and the NVFP4 8192^3 GEMM on prepacked weights, and
+    one step of the decoder-layer sweep (every projection and the LM head at
+    M = 1, 16, 128, 2048).  Each: a warmed CUDA graph of back-to-back calls
+    (weight copies rotated past L2), CUDA events with a spin kernel ahead of
+    the start, its own clock samples.  Not part of the value."""
+    import torch
+    import weight_only_bit_w4a16_gb300 as wq
+    from weight_only_bit_w4a16_gb300 import metrics
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 * 1024 * 1024)
+    s = torch.cuda.Stream(dev)
+    out = {}
+
+    def timed(g_, n_calls, reps):
+        g_.replay()
+        torch.cuda.synchronize()
+        sampler = ClockSampler(gpu_id)
+        time.sleep(0.2)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.monotonic()
+        with torch.cuda.stream(s):
+            torch.cuda._sleep(SPIN_CYCLES)
+            e0.record(s)
+            for _ in range(reps):
+                g_.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        t1 = time.monotonic()
+        time.sleep(0.1)
+        sampler.stop()
+        return e0.elapsed_time(e1) / (reps * n_calls), sampler.summary(t0, t1)
+
+    for name in ("prefill_mxfp4", "large_nvfp4"):
+        w = BENCH_WORKLOADS[name]
+        fmt, group, N, K, M = w["fmt"], w["group"], w["N"], w["K"], w["Ms"][0]
+        A_by_M, (pk_h, sc_h, zr_h) = host_inputs(w)
+        wb = metrics.weight_bytes(fmt, N, K, group)
+        R = max(2, math.ceil(2.0 * l2 / wb))
+        pk = torch.from_numpy(pk_h).to(dev)
+        sc = torch.from_numpy(sc_h).to(dev)
+        pres = [wq.prepack(pk, sc, None, fmt, group) for _ in range(R)]
+        torch.cuda.synchronize()
+        del pk, sc
+        A = torch.from_numpy(A_by_M[M].view(np.int16)).view(torch.bfloat16).to(dev)
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        wsb = wq.wq_gemm_workspace_size(M, N, K, wq.FORMATS[fmt], group)
+        work = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
+        n_calls = R * max(1, math.ceil(8 / R))
+        with torch.cuda.stream(s):
+            def go(i, h):
+                st = wq.wq_gemm_prepacked(A.data_ptr(), pres[i % R].buf.data_ptr(), C.data_ptr(), M, N, K,
+                                          wq.FORMATS[fmt], group, None, work.data_ptr(), wsb, h, wq.WQ_PATH_AUTO)
+                if st != wq.WQ_OK:
+                    raise wq.WQError(st, name)
+            go(0, s.cuda_stream)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for i in range(n_calls):
+                    go(i, torch.cuda.current_stream().cuda_stream)
+        reps = max(1, math.ceil(0.1 / max(1e-6, n_calls * 2.0 * M * N * K / 1.5e15)))
+        ms, clk = timed(g, n_calls, reps)
+        flops = 2.0 * M * N * K
+        tf = flops / (ms / 1e3) / 1e12
+        out[name] = {"M": M, "N": N, "K": K, "format": fmt, "ms_per_call": ms, "tflops": tf, "calls": n_calls * reps,
+                     "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                  "frac": tf / peaks["bf16_tflops"],
+                                  "peak_source": peaks["source"] + " bf16_tflops (burst)"},
+                     "clocks": clk, "layout": "prepacked", "rotation": f"{R} weight copies"}
+        del g, pres, A, C, work
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+    # one step of the decoder-layer sweep: every projection and the LM head
+    # at every M, chained (the small-M calls with their inputs ready)
+    w = BENCH_WORKLOADS["layer_sweep"]
+    shapes = sweep_shapes(w)
+    weights_h, A_h = sweep_inputs(w, shapes)
+    pres = {c: wq.prepack(torch.from_numpy(pk).to(dev), torch.from_numpy(sc.view(np.int16)).to(dev),
+                          torch.from_numpy(zr).to(dev), "int4", 128) for c, (pk, sc, zr) in weights_h.items()}
+    torch.cuda.synchronize()
+    A_d = {k: torch.from_numpy(a.view(np.int16)).to(dev) for k, a in A_h.items()}
+    C_d = {(M, c): torch.empty((M, N), dtype=torch.bfloat16, device=dev) for M in w["Ms"] for c, (N, K) in shapes.items()}
+    wsb = max(wq.wq_gemm_workspace_size(M, N, K, wq.WQ_INT4, 128) for M in w["Ms"] for N, K in shapes.values())
+    work = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
+    flags = LAUNCH_FLAGS[args.launch](wq)
+
+    def step(h):
+        for M in w["Ms"]:
+            for c, (N, K) in shapes.items():
+                st = wq.wq_gemm_prepacked(A_d[(M, K)].data_ptr(), pres[c].buf.data_ptr(), C_d[(M, c)].data_ptr(), M,
+                                          N, K, wq.WQ_INT4, 128, None, work.data_ptr(), wsb, h,
+                                          wq.WQ_PATH_AUTO | flags)
+                if st != wq.WQ_OK:
+                    raise wq.WQError(st, f"{c} M={M}")
+
+    with torch.cuda.stream(s):
+        step(s.cuda_stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step(torch.cuda.current_stream().cuda_stream)
+    ms, clk = timed(g, 1, 20)
+    bound = sum(roofline_time(M, N, K, peaks)[0] for M in w["Ms"] for N, K in shapes.values())
+    flops = sum(2.0 * M * N * K for M in w["Ms"] for N, K in shapes.values())
+    out["layer_sweep_step"] = {"calls": len(w["Ms"]) * len(shapes), "ms_per_step": ms,
+                               "roofline_ms": bound * 1e3, "pct_of_roofline": 100.0 * bound / (ms / 1e3),
+                               "tflops": flops / (ms / 1e3) / 1e12, "steps": 20, "clocks": clk,
+                               "launch": LAUNCH_DESC[args.launch] + " for the small-M calls"}
+    del g, pres, A_d, C_d, work
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -673,7 +852,10 @@ def run_e2e(args, w, A_by_M, weights, pool, dev, ws, pre_pool=None):
     s = torch.cuda.Stream(dev)
     R = len(pool)
     steps = max(1, min(args.steps, 2000))
-    overlap = not args.no_overlap
+    # the step's first call follows the copy of its activations (a full
+    # dependency); the others launch as the timed steps do (their A arrived
+    # with the same copy, complete before the first call began)
+    kw_later = {"overlap": args.launch != "plain", "inputs_ready": args.launch == "ready"}
 
     def one(i, upload_weights=None):
         if upload_weights is not None:
@@ -689,11 +871,12 @@ def run_e2e(args, w, A_by_M, weights, pool, dev, ws, pre_pool=None):
         A_d_all.copy_(A_h_all, non_blocking=True)
         for j, M in enumerate(Ms):
             slot = (i * len(Ms) + j) % R
+            kw = kw_later if j > 0 else {}
             if pre_pool is not None:
-                wq.gemm_prepacked(A_d[M], pre_pool[slot], out_dtype=out, out=C_d[M], overlap=overlap and j > 0)
+                wq.gemm_prepacked(A_d[M], pre_pool[slot], out_dtype=out, out=C_d[M], **kw)
             else:
                 pk, sc, zr = pool[slot]
-                wq.gemm(A_d[M], pk, sc, zr, fmt, group, out_dtype=out, out=C_d[M], overlap=overlap and j > 0)
+                wq.gemm(A_d[M], pk, sc, zr, fmt, group, out_dtype=out, out=C_d[M], **kw)
         C_h_all.copy_(C_d_all, non_blocking=True)
 
     def timed(nsteps, upload=None):
@@ -740,11 +923,12 @@ def run_e2e(args, w, A_by_M, weights, pool, dev, ws, pre_pool=None):
         vA, vC = views[b_]
         for j, M in enumerate(Ms):
             slot = (i * len(Ms) + j) % R
+            kw = kw_later if j > 0 else {}
             if pre_pool is not None:
-                wq.gemm_prepacked(vA[M], pre_pool[slot], out_dtype=out, out=vC[M], overlap=overlap and j > 0)
+                wq.gemm_prepacked(vA[M], pre_pool[slot], out_dtype=out, out=vC[M], **kw)
             else:
                 pk, sc, zr = pool[slot]
-                wq.gemm(vA[M], pk, sc, zr, fmt, group, out_dtype=out, out=vC[M], overlap=overlap and j > 0)
+                wq.gemm(vA[M], pk, sc, zr, fmt, group, out_dtype=out, out=vC[M], **kw)
 
     def p_d2h(i, b_):
         C_hb[b_].copy_(C_buf[b_], non_blocking=True)
@@ -813,8 +997,7 @@ def run_reference(args):
            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3 / args.steps,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic",
-           "config": {"workload": args.workload, "format": w["fmt"], "group": w["group"], "M": list(w["Ms"]),
-                      "N": w["N"], "K": w["K"], "out": w["out"]},
+           "config": bench_config(args.workload, ws),
            "cpu_baseline": {"value": value, "unit": w["unit"], "cores": oracle.max_threads(),
                             "kind": "oracle", "sample": sample, "cpu": cpu_model()},
            "e2e": {"value": value, "unit": w["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -887,7 +1070,7 @@ def run_sweep(args):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 128 * 1024 * 1024)
     prepacked = args.layout == "prepacked"
-    overlap = 0 if args.no_overlap else wq.WQ_LAUNCH_OVERLAP
+    overlap = LAUNCH_FLAGS[args.launch](wq)
 
     weights_h, A_h = sweep_inputs(w, shapes)
 
@@ -1043,17 +1226,14 @@ def run_sweep(args):
         "metric": w["metric"], "value": value, "unit": w["unit"], "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "format": fmt, "group": group, "M": list(Ms),
-                   "calls": {c: list(shapes[c]) for c in shapes}, "out": "bf16",
-                   "calls_per_step": len(Ms) * len(shapes),
-                   "l2": f"inputs larger than L2: a step streams {wbytes_step / 1e6:.0f} MB of weights per M "
-                         f"(L2 {l2 / 1e6:.0f} MB); a weight is reused only after all the others",
-                   "timing": "CUDA graph of one step, replayed; CUDA events on the launching stream",
-                   "launch": "WQ_LAUNCH_OVERLAP (programmatic dependent launch)" if overlap else "plain",
-                   "layout": ("prepacked (wq_prepack, untimed build step)" if prepacked else
-                              "as given (packed, scales, zeros)"),
-                   "workspace": f"{ws_bytes} B, shared by the calls (stream-K where the tiles fill the SMs badly)",
-                   "parallelism": f"replicas x{ws}"},
+        "config": bench_config(args.workload, ws),
+        "setup": {"l2": f"inputs larger than L2: a step streams {wbytes_step / 1e6:.0f} MB of weights per M "
+                        f"(L2 {l2 / 1e6:.0f} MB); a weight is reused only after all the others",
+                  "timing": "CUDA graph of one step, replayed; CUDA events on the launching stream",
+                  "launch": LAUNCH_DESC[args.launch] + " (small-M calls; the tensor-core path ignores it)",
+                  "layout": ("prepacked (wq_prepack, untimed build step)" if prepacked else
+                             "as given (packed, scales, zeros)"),
+                  "workspace": f"{ws_bytes} B, shared by the calls (stream-K where the tiles fill the SMs badly)"},
         "roofline": roof, "clocks": clocks, "gpu_launches": args.steps * len(Ms) * len(shapes), "e2e": e2e,
         "step": {"roofline_us": bound_step * 1e6, "measured_us": step_s * 1e6,
                  "tflops": flops_step / step_s / 1e12},
@@ -1126,13 +1306,13 @@ def run_sweep_e2e(args, w, shapes, weights_h, A_h, wsets, prepacked, dev, ws, bo
         j = 0
         for M in Ms:
             for c, (N, K) in shapes.items():
-                ov = not args.no_overlap and j > 0
+                kw = ({"overlap": args.launch != "plain", "inputs_ready": args.launch == "ready"} if j > 0 else {})
                 wsp = big if work[(M, c)] is not None else None
                 if prepacked:
-                    wq.gemm_prepacked(vA[(M, K)], wsets[c], out=vC[(M, c)], overlap=ov, workspace=wsp)
+                    wq.gemm_prepacked(vA[(M, K)], wsets[c], out=vC[(M, c)], workspace=wsp, **kw)
                 else:
                     pk, sc, zr = wsets[c]
-                    wq.gemm(vA[(M, K)], pk, sc, zr, "int4", out=vC[(M, c)], overlap=ov, workspace=wsp)
+                    wq.gemm(vA[(M, K)], pk, sc, zr, "int4", out=vC[(M, c)], workspace=wsp, **kw)
                 j += 1
 
     def d2h(i, b):
@@ -1178,8 +1358,7 @@ def run_reference_sweep(args):
     res = {"impl": "reference", "metric": w["metric"], "value": value, "unit": w["unit"],
            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3 / args.steps,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": args.workload, "format": w["fmt"], "group": w["group"], "M": list(w["Ms"]),
-                      "calls": {c: list(shapes[c]) for c in shapes}, "out": w["out"]},
+           "config": bench_config(args.workload, ws),
            "cpu_baseline": {"value": value, "unit": w["unit"], "cores": oracle.max_threads(),
                             "kind": "oracle", "sample": sample, "cpu": cpu_model()},
            "e2e": {"value": value, "unit": w["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -1196,11 +1375,16 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS), default="decode_int4")
     ap.add_argument("--layout", choices=["prepacked", "plain"], default="prepacked",
                     help="weights as given, or repacked once by wq_prepack before timing")
-    ap.add_argument("--no-overlap", action="store_true",
-                    help="time plain launches instead of WQ_LAUNCH_OVERLAP")
+    ap.add_argument("--launch", choices=sorted(LAUNCH_FLAGS), default="ready",
+                    help="launch mode of the small-M calls: inputs ready (default), dependent chain, plain")
+    ap.add_argument("--no-overlap", action="store_true", help="same as --launch plain")
+    ap.add_argument("--no-tensor-core", action="store_true",
+                    help="skip the tensor-core block of the default (decode) run")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     args = ap.parse_args(argv)
+    if args.no_overlap:
+        args.launch = "plain"
     d_steps, d_warm = DEFAULT_STEPS.get(args.workload, (20000, 200))
     args.steps = d_steps if args.steps is None else args.steps
     args.warmup = d_warm if args.warmup is None else args.warmup

@@ -41,3 +41,20 @@ def test_roofline_time_takes_the_larger_bound():
     # 0.79 + 4.94 + 0.79 MB of A, weights and C (0.82 us at 8 TB/s)
     t, bound = bench.roofline_time(128, 3072, 3072, PEAKS)
     assert bound == "tensor" and abs(t - 2 * 128 * 3072 * 3072 / 2e15) < 1e-15
+
+
+def test_both_arms_describe_the_same_workload():
+    """The config of a line names the workload only, so our arm and the
+    reference arm build the same dict (how our arm launches and lays out its
+    weights goes under "setup")."""
+    import inspect
+    for name in bench.BENCH_WORKLOADS:
+        cfg = bench.bench_config(name, 1)
+        assert cfg["workload"] == name and cfg["parallelism"] == "replicas x1"
+        assert {"format", "group", "M", "out", "calls_per_step"} <= set(cfg)
+    src_ours, src_ref = inspect.getsource(bench.run_ours), inspect.getsource(bench.run_reference)
+    assert '"config": bench_config(args.workload, ws)' in src_ours
+    assert '"config": bench_config(args.workload, ws)' in src_ref
+    assert bench.bench_config("decode_int4", 1) == {
+        "workload": "decode_int4", "format": "int4", "group": 128, "M": [1, 4, 16], "out": "bf16",
+        "N": 8192, "K": 3072, "calls_per_step": 3, "parallelism": "replicas x1"}

@@ -148,10 +148,15 @@ int wq_gemm_ws(const void* A, const uint8_t* packed, const void* scales, const u
  * allocates nothing.  The method itself has no such step; it exists so that
  * a caller without a memory allocator still gets the balanced tensor-core
  * path.  Limits: one scratch per device, so calls through this entry point
- * must be ordered on the device (one stream at a time), and a shape whose
- * split would need more scratch than the array holds returns
+ * must be ordered on the device (one stream at a time), and a tensor-core
+ * call whose split would need more scratch than the array holds returns
  * WQ_ERR_UNSUPPORTED without launching (WQ_STATIC_WS_CAP in the environment
- * lowers the usable size, for tests).  Otherwise as wq_gemm_ex.
+ * lowers the usable size, for tests); calls that run on the small-M kernel
+ * use no scratch.  Recovery: a call whose bounded wait ran out leaves flag
+ * words set in the scratch; once wq_get_device_error() has returned that
+ * WQ_ERR_DEVICE_TIMEOUT, the next wq_gemm_static call on the device first
+ * zeroes them with a memset on its stream (nothing is allocated).
+ * Otherwise as wq_gemm_ex.
  */
 int wq_gemm_static(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
                    void* C, int M, int N, int K, int format, int group, void* stream, int path);
@@ -276,7 +281,14 @@ int wq_dequant(const uint8_t* packed, const void* scales, const uint8_t* zeros, 
                int N, int K, int format, int group, void* stream);
 
 /* Returns the device status word (WQ_OK or WQ_ERR_DEVICE_TIMEOUT) of the
- * current device and clears it.  Synchronises the device. */
+ * current device and clears it.  Synchronises the device.  A timeout it
+ * returns also marks the library scratch of wq_gemm_static for clearing.
+ * Tests can run the tensor-core kernel's failure path on purpose:
+ * WQ_TC_FLAG_WAIT_NS in the environment (read at each launch) bounds a
+ * stream-K tile owner's wait for its contributors' partial sums, and 0 makes
+ * every such wait give up at once; the kernel then unwinds (its copies and
+ * MMAs drain under their own bounds), records the timeout and stores
+ * nothing for the tiles whose wait gave up. */
 int wq_get_device_error(void);
 
 /* Failure-path self test: enqueues a one-thread kernel whose bounded wait on

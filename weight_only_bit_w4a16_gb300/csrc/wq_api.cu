@@ -97,15 +97,24 @@ WQ_EXPORT int wq_gemm_ws(const void* A, const uint8_t* packed, const void* scale
 
 WQ_EXPORT int wq_gemm_static(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
                              void* C, int M, int N, int K, int format, int group, void* stream, int path) {
+    // the description first, as every entry point checks it
+    if (format & ~(0xFF | WQ_OUT_F32)) return WQ_ERR_INVALID_ARG;
+    if (M < 0) return WQ_ERR_INVALID_ARG;
+    if (path & ~(0xFF | WQ_LAUNCH_OVERLAP | WQ_LAUNCH_INPUTS_READY)) return WQ_ERR_INVALID_ARG;
+    const int route = path & 0xFF;
+    if (route != WQ_PATH_AUTO && route != WQ_PATH_GEMV && route != WQ_PATH_TC) return WQ_ERR_INVALID_ARG;
+    int st = check_weights(packed, scales, zeros, N, K, format & 0xFF, group);
+    if (st != WQ_OK) return st;
     size_t cap = 0;
-    void* ws = wq::static_workspace(&cap);
-    if (!ws) return WQ_ERR_CUDA;
+    void* ws = wq::static_workspace(&cap, static_cast<cudaStream_t>(stream), &st);
+    if (!ws) return st != WQ_OK ? st : WQ_ERR_CUDA;
     if (const char* e = getenv("WQ_STATIC_WS_CAP")) {   // tests: a smaller usable part
         const size_t v = (size_t)strtoull(e, nullptr, 10);
         if (v < cap) cap = v;
     }
-    const size_t need =
-        (M > 16 && N > 0 && K > 0 && K % 64 == 0) ? wq::tc_workspace_bytes(M, N, K, format & 0xFF) : 0;
+    // the scratch matters only where the tensor-core kernel runs
+    const bool tc = route == WQ_PATH_TC || (route == WQ_PATH_AUTO && M > 16);
+    const size_t need = (tc && N > 0 && K > 0 && K % 64 == 0) ? wq::tc_workspace_bytes(M, N, K, format & 0xFF) : 0;
     if (need > cap) return WQ_ERR_UNSUPPORTED;
     return gemm_impl(A, packed, scales, zeros, C, M, N, K, format, group, ws, cap, stream, path);
 }

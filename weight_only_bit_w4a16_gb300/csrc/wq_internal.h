@@ -60,8 +60,10 @@ int launch_gemv_staged(const void* A, const void* prepacked, void* C, int M, int
 
 // The library's own stream-K scratch (a file-scope device array of the
 // tensor-core module) on the current device and its size; NULL if the
-// address cannot be had.
-void* static_workspace(size_t* bytes);
+// address cannot be had (status WQ_ERR_CUDA).  After a call reported a
+// timeout (read_and_clear_device_status), it first zeroes the scratch's flag
+// words on `stream`.
+void* static_workspace(size_t* bytes, cudaStream_t stream, int* status);
 
 // A kernel whose bounded wait is bound to run out (tests the failure path).
 int launch_timeout_selftest(cudaStream_t stream);

@@ -48,12 +48,22 @@ namespace wq {
 // WQ_OK, or WQ_ERR_DEVICE_TIMEOUT once a bounded wait of a kernel gave up.
 __device__ int g_device_status = 0;
 
+// Devices whose library scratch (wq_gemm_static) may hold flags a timed-out
+// call left set: a wait that ran out leaves its tile's flags as they were.
+static bool g_static_dirty[64];
+static std::mutex g_static_mu;
+
 int read_and_clear_device_status() {
     int v = 0;
     const int zero = 0;
     if (cudaDeviceSynchronize() != cudaSuccess) return WQ_ERR_CUDA;
     if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return WQ_ERR_CUDA;
     if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return WQ_ERR_CUDA;
+    int dev = 0;
+    if (v != 0 && cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+        std::lock_guard<std::mutex> lock(g_static_mu);
+        g_static_dirty[dev] = true;
+    }
     return v;
 }
 
@@ -102,6 +112,7 @@ struct TcArgs {
     int kblocks;        // prepacked weights: 128-k blocks per row
     int vec_store;      // C rows 16-byte aligned and the store scratch allocated: vector stores of C
     int scr_off;        // byte offset of the decode warps' store scratch (2 KB each) in shared memory
+    unsigned long long flag_wait_ns;   // bound of a stream-K owner's wait for a partial (0: give up at once)
     Epilogue epi;
 };
 
@@ -329,7 +340,13 @@ __device__ __forceinline__ float4* partial_ptr(const TcArgs& a, int slot, int ch
     return reinterpret_cast<float4*>(a.ws) + (((size_t)slot * (a.bm / 32) + ch) * 8 + j) * kBN + row;
 }
 
+// A limit of 0 gives up at once without reading the flag (the host sets it
+// only to run the failure path in tests; see WQ_TC_FLAG_WAIT_NS).
 __device__ __forceinline__ bool wait_flag(const unsigned* f, volatile int* abort, uint64_t limit_ns) {
+    if (limit_ns == 0) {
+        *abort = 1;
+        return false;
+    }
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 0;; ++i) {
         unsigned v;
@@ -576,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c0 = cfirst; c0 < cta && ok; c0 += 32) {
                     const int c2 = c0 + lane;
                     const bool mine = c2 < cta;
-                    const bool got = !mine || wait_flag(a.flags + c2, abort, kWaitNs);
+                    const bool got = !mine || wait_flag(a.flags + c2, abort, a.flag_wait_ns);
                     ok = __all_sync(0xffffffffu, got);
                 }
             }
@@ -939,14 +956,23 @@ constexpr int kStaticCtas = 160;
 constexpr size_t kStaticWsBytes = kFlagBytes(kStaticCtas) + (size_t)kStaticCtas * kBN * kBMMax * sizeof(float);
 static __device__ __align__(256) uint8_t g_static_ws[kStaticWsBytes];
 
-void* static_workspace(size_t* bytes) {
-    static std::mutex mu;
+void* static_workspace(size_t* bytes, cudaStream_t stream, int* status) {
     static void* addr[64] = {};
+    *status = WQ_OK;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
+    std::lock_guard<std::mutex> lock(g_static_mu);
     if (!addr[dev] && cudaGetSymbolAddress(&addr[dev], g_static_ws) != cudaSuccess) addr[dev] = nullptr;
     *bytes = addr[dev] ? kStaticWsBytes : 0;
+    if (addr[dev] && g_static_dirty[dev]) {
+        // a call reported a timeout since: zero the flag words before this
+        // call's kernel reads them (on its stream; nothing is allocated)
+        if (cudaMemsetAsync(addr[dev], 0, kFlagBytes(kStaticCtas), stream) != cudaSuccess) {
+            *status = WQ_ERR_CUDA;
+            return nullptr;
+        }
+        g_static_dirty[dev] = false;
+    }
     return addr[dev];
 }
 
@@ -1001,6 +1027,8 @@ int run_tc(const void* A, const CUtensorMap& tp, bool pre, const uint8_t* scales
     args.units = plan.units;
     args.G = plan.G;
     args.kblocks = kblocks;
+    args.flag_wait_ns = kWaitNs;
+    if (const char* e = getenv("WQ_TC_FLAG_WAIT_NS")) args.flag_wait_ns = strtoull(e, nullptr, 10);   // tests
     args.epi = epi;
     if (debug_on())
         fprintf(stderr, "wq: tcgen05%s M=%d N=%d K=%d: bm=%d tiles=%d %s grid=%d\n", pre ? " (prepacked)" : "", M, N,

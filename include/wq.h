@@ -194,6 +194,10 @@ int wq_gemm_fused(const void* A, const uint8_t* packed, const void* scales, cons
  * invalid description). */
 size_t wq_gemm_workspace_size(int M, int N, int K, int format, int group);
 
+/* The same size under the name the library's design gives it (an alias of
+ * wq_gemm_workspace_size). */
+size_t wq_workspace_bytes(int M, int N, int K, int format, int group);
+
 /*
  * Offline repack ("prepack").  The KBench spec's build step may put the
  * weights in any layout ("interleaved nibbles, pre-swizzled for your MMA

@@ -163,3 +163,9 @@ def test_gemm_prepacked_argument_checks():
     assert f(FAKE, FAKE, FAKE, 4, 32, 256, 0, 16, ws=ODD, wsb=64) == wq.WQ_ERR_ALIGN
     epi = wq.wq_epilogue(None, None, 1)
     assert f(FAKE, FAKE, FAKE, 4, 24, 256, 0, 16, ctypes.byref(epi)) == wq.WQ_ERR_UNSUPPORTED
+
+
+def test_workspace_size_alias():
+    """wq_workspace_bytes is wq_gemm_workspace_size under its design name."""
+    for args in ((300, 3072, 3072, 2, 128), (4, 512, 1024, 2, 128), (0, 8, 64, 0, 16), (300, 1000, 1024, 1, 32)):
+        assert wq.wq_workspace_bytes(*args) == wq.wq_gemm_workspace_size(*args)

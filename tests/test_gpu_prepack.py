@@ -429,6 +429,27 @@ def test_tc_fused_epilogue():
     assert not (np.abs(Y - Ye) > T).any()
 
 
+def test_tc_large_nvfp4_prepacked():
+    """The bench's own large-M instance: 8192^3 NVFP4 through
+    gemm_prepacked(A, prepack(...)) with the default plan (tiles of 256 rows
+    on persistent CTAs, the plain instance).  64 random rows (all 8192
+    columns) and 64 random columns (all 8192 rows), plus the first and last
+    of each, against the oracle on the original weight."""
+    p = synth.workload_problem("large_nvfp4")
+    A, _, _, _ = to_dev(p)
+    pre = prepack_dev(p)
+    C = wq.gemm_prepacked(A, pre)
+    torch.cuda.synchronize()
+    assert wq.wq_get_device_error() == wq.WQ_OK
+    rows, cols = sample(8192, 64, 0), sample(8192, 64, 1)
+    Cr, Cc = host_rows_cols(C, rows, cols)
+    del C, A, pre
+    Ce, S = oracle_ref(p, rows=rows)
+    assert_parity(Cr, Ce, S, "bf16", "large_nvfp4 prepacked rows")
+    Ce, S = oracle_ref(p, cols=cols)
+    assert_parity(Cc, Ce, S, "bf16", "large_nvfp4 prepacked cols")
+
+
 def test_tc_prefill_workload_full_size():
     """The prefill configuration (MXFP4, M = 2048, N = K = 3072, bf16 out) on
     prepacked weights: oracle on sampled rows and columns."""

@@ -49,6 +49,7 @@ SIGNATURES = {
     "wq_gemm_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i]),
     "wq_gemm_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, ctypes.c_size_t, _vp, _i]),
     "wq_gemm_workspace_size": (ctypes.c_size_t, [_i, _i, _i, _i, _i]),
+    "wq_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i]),
     "wq_gemm_static": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i]),
     "wq_gemm_fused": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(wq_epilogue), _vp,
                            ctypes.c_size_t, _vp, _i]),
@@ -119,6 +120,10 @@ def wq_gemm_fused(A, packed, scales, zeros, C, M, N, K, format, group, epilogue,
 
 def wq_gemm_workspace_size(M, N, K, format, group) -> int:
     return lib().wq_gemm_workspace_size(M, N, K, format, group)
+
+
+def wq_workspace_bytes(M, N, K, format, group) -> int:
+    return lib().wq_workspace_bytes(M, N, K, format, group)
 
 
 def wq_prepack_bytes(N, K, format, group) -> int:

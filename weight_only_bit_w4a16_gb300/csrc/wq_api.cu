@@ -135,6 +135,10 @@ WQ_EXPORT size_t wq_gemm_workspace_size(int M, int N, int K, int format, int gro
     return wq::tc_workspace_bytes(M, N, K, format & 0xFF);
 }
 
+WQ_EXPORT size_t wq_workspace_bytes(int M, int N, int K, int format, int group) {
+    return wq_gemm_workspace_size(M, N, K, format, group);
+}
+
 WQ_EXPORT int wq_gemm(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C, int M,
             int N, int K, int format, int group) {
     return wq_gemm_ex(A, packed, scales, zeros, C, M, N, K, format, group, nullptr, WQ_PATH_AUTO);

@@ -4,7 +4,7 @@
  * The library computes  C = A . deq(B)^T  on one NVIDIA GB300 (sm_103a):
  *
  *   A        (M, K)   bf16 activations, row-major.
- *   packed   (N, K/2) uint8, two 4-bit codes per byte; byte j of row n holds
+ *   packed   (N, K/2) uint8, a pair of 4-bit codes in each byte; byte j of row n holds
  *            element k = 2j in its LOW nibble and k = 2j+1 in its HIGH
  *            nibble (KBench megakernel_int4_weight_decode.py spec, "The
  *            weight format"; TileLang example_dequant_gemm_bf16_fp4_hopper.py,
@@ -199,10 +199,10 @@ size_t wq_gemm_workspace_size(int M, int N, int K, int format, int group);
 size_t wq_workspace_bytes(int M, int N, int K, int format, int group);
 
 /*
- * Offline repack ("prepack").  The KBench spec's build step may put the
- * weights in any layout ("interleaved nibbles, pre-swizzled for your MMA
- * fragment, scales hoisted into a separate stream"), as long as what is
- * streamed per call is still the 4-bit codes.  wq_prepack writes such a
+ * Offline repack ("prepack").  The KBench spec's untimed build step may store
+ * the weights in whatever layout suits the kernel (nibble order, fragment
+ * order, scales apart from the codes) as long as what is streamed per call
+ * is still the 4-bit codes.  wq_prepack writes such a
  * layout once; wq_gemm_prepacked then computes the same C as wq_gemm_fused
  * on the original arrays, reading only the prepacked buffer.
  *

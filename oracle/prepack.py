@@ -2,10 +2,10 @@
 
 TEST INFRASTRUCTURE ONLY (see the package docstring): nothing in the product
 library imports this module, and it shares no code with the library's repack
-kernel.  The layout is a build-step choice that the KBench spec allows ("You
-may repack the weights into any layout you like" in the untimed build step:
-interleaved nibbles, fragment pre-swizzle, scales in their own stream); its
-definition is the one stated above ``wq_prepack_bytes`` in ``include/wq.h``,
+kernel.  The layout is a build-step choice the KBench spec leaves open (its
+untimed build step may store the weights however the kernel likes best, for
+example with nibbles interleaved, pre-arranged for the MMA fragments and the
+scales in a stream of their own); its definition is the one stated above ``wq_prepack_bytes`` in ``include/wq.h``,
 restated here:
 
 * codes: ``Nb = ceil(N/16)`` row blocks x ``I = ceil(K/128)`` k-blocks of

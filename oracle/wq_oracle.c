@@ -27,10 +27,10 @@
  *        (N, K/2) uint8, scales (N, K/16) float8_e4m3fn, weight =
  *        decode_e2m1 * |scale|.
  *   [P4] megakernel_int4_weight_decode.py (KBench task spec), "The weight
- *        format" and the Precision section: packed (out, in/2) uint8 with the
- *        LOW nibble holding the EVEN input index, scale (out, in/group) bf16,
- *        zero (out, in/group) uint8, value = (code - zero) * scale, subtract
- *        before multiply, group = 128 contiguous input elements.
+ *        format" and the Precision section: two codes per uint8, the even
+ *        input index in the low nibble; per group of 128 consecutive inputs a
+ *        bf16 scale and a uint8 zero point; value = (code - zero) * scale,
+ *        the zero point subtracted first.
  *   MXFP4 uses the OCP Microscaling (MX) definition of the scale: an e8m0
  *   byte E meaning 2^(E-127), 0xFF = NaN, one scale per 32 elements.
  *

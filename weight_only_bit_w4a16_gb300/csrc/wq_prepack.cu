@@ -2,9 +2,9 @@
 // defined above wq_prepack_bytes in include/wq.h.
 //
 // The KBench megakernel_int4_weight_decode.py spec lets the untimed build
-// step put the weights in any layout ("interleaved nibbles, pre-swizzled for
-// your MMA fragment, scales hoisted into a separate stream") as long as the
-// 4-bit codes are what is streamed per call.  This layout serves the small-M
+// step store the weights in whatever layout suits the kernel (nibble order,
+// fragment order, scales apart from the codes) as long as the 4-bit codes
+// are what is streamed per call.  This layout serves the small-M
 // kernel (wq_gemv_pre.cu):
 //   - a 16-row x 128-k block is 1024 contiguous bytes, so a warp's whole
 //     slice (16 rows x its k range) is one bulk copy, with no row padding;

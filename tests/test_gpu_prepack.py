@@ -130,7 +130,7 @@ def _ring_smem(fmt, M, K, RB, Wk, P):
     mrows = 16 if M > 8 else 8
     Mc, MP = min(M, mrows), (16 if M > 8 else 8)
     ring_off = r128(8 * Wk * P)
-    slot = r128(1024 * RB + 320 * Mc)
+    slot = r128(1024 * RB + 256 * Mc)
     end = ring_off + Wk * P * slot + Wk * RB * ipw * (96 if fmt == "int4" else 512)
     red = ring_off + Wk * MP * (RB * 16 + 4) * 4
     return max(end, red) + 128

@@ -33,7 +33,7 @@
 // Shared memory (from a 128-byte aligned base):
 //   bars  [Wk][P] u64 at 0                     slot landed (32 arrivals)
 //   ring  [Wk][P][slot_bytes] at ring_off      RB code blocks, then the
-//                                              activation rows, kAStride apart
+//                                              activation rows (256 B, swizzled)
 //   recs  [Wk][RB][ipw][96]  int4 at rec_off   the copied record blocks
 //         [Wk][RB][ipw][512] fp4               decoded multipliers, per lane
 //   red   [Wk][MP][RB*16 + 4] f32 at ring_off  partial sums (aliases ring/recs)
@@ -68,8 +68,11 @@ using namespace sm100;
 
 constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s: far above any legal wait
 constexpr int kMaxWkLog2 = 3;                           // K ranges (warps) per CTA <= 8
-constexpr uint32_t kAStride = 320;   // activation row stride in a slot: 256 + 64, so that the
-                                     // rows a quarter-warp reads sit in opposite bank halves
+// Activation rows in a slot are 256 bytes apart (128 k), their 16-byte units
+// swizzled: unit u of row m sits at position u ^ (4 (m & 1)).  The lanes of a
+// quarter-warp read units c + 4j of two adjacent rows, which then fall in
+// opposite 64-byte halves of a 128-byte window: no bank conflict, no padding.
+constexpr uint32_t kAStride = 256;
 
 struct PreArgs {
     const uint8_t* codes;   // code blocks
@@ -239,6 +242,64 @@ __device__ __forceinline__ void step_int4(uint32_t wp, uint32_t rec, uint32_t r,
     }
 }
 
+// int4 g128, row blocks q0 .. q0 + QI - 1 of a step, their MMA chains
+// interleaved word by word (independent accumulators in flight together).
+// rec0: record block of row block 0 of this step; rec_stride: bytes between
+// the record blocks of consecutive row blocks.
+template <int NT, int QI, bool TWO>
+__device__ __forceinline__ void step_int4_group(uint32_t wp0, uint32_t rec0, uint32_t rec_stride, uint32_t r,
+                                                const uint4 (&bv)[NT][4], float (*acc)[NT][4]) {
+    uint32_t wa[QI][4], wb[QI][4], zzA[QI], zzB[QI], zzA2[QI], zzB2[QI];
+    float sa[QI], sb[QI];
+#pragma unroll
+    for (int q = 0; q < QI; ++q) {
+        uint4 qa, qb;
+        block_words(wp0 + 1024u * q, qa, qb);
+        wa[q][0] = qa.x; wa[q][1] = qa.y; wa[q][2] = qa.z; wa[q][3] = qa.w;
+        wb[q][0] = qb.x; wb[q][1] = qb.y; wb[q][2] = qb.z; wb[q][3] = qb.w;
+        const uint32_t rec = rec0 + rec_stride * q;
+        const uint2 rr = lds64(rec + 8u * r);
+        zzA[q] = prmt(rr.x, rr.x, 0x3232u);
+        zzB[q] = prmt(rr.y, rr.y, 0x3232u);
+        sa[q] = __uint_as_float(rr.x << 16);
+        sb[q] = __uint_as_float(rr.y << 16);
+        zzA2[q] = zzB2[q] = 0;
+        if constexpr (TWO) {
+            const uint32_t z2 = lds32(rec + 64u + 4u * r);
+            zzA2[q] = splat16(z2);
+            zzB2[q] = splat16(z2 >> 16);
+        }
+    }
+    // CH independent MMA chains per tile and row block (words j = h mod CH)
+    constexpr int CH = NT == 1 ? 2 : 1;
+    float part[QI][CH][NT][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int q = 0; q < QI; ++q) {
+            uint32_t pa[4], pb[4];
+            int4_word_kk4<TWO>(wa[q][j], zzA[q], zzA2[q], pa);
+            int4_word_kk4<TWO>(wb[q][j], zzB[q], zzB2[q], pb);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                if (j < CH) mma16816_z(part[q][j % CH][t], pa[0], pb[0], pa[1], pb[1], bv[t][j].x, bv[t][j].y);
+                else mma16816(part[q][j % CH][t], pa[0], pb[0], pa[1], pb[1], bv[t][j].x, bv[t][j].y);
+                mma16816(part[q][j % CH][t], pa[2], pb[2], pa[3], pb[3], bv[t][j].z, bv[t][j].w);
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < QI; ++q)
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float p = part[q][0][t][e];
+                if constexpr (CH == 2) p += part[q][CH - 1][t][e];
+                acc[q][t][e] = fmaf(e < 2 ? sa[q] : sb[q], p, acc[q][t][e]);
+            }
+}
+
 // fp4, one row block of a step.  rp: the lane's decoded multipliers, words
 // j = 0..3 of row r (16 bytes) then of row r + 8; the second multipliers
 // (MXFP4 scales above 2^15) 256 bytes on.
@@ -285,7 +346,8 @@ __device__ __forceinline__ void step_fp4(uint32_t wp, uint32_t rp, const uint4 (
 //   rlane  : the lane's offset in a record block (int4: its row r)
 template <int FMT, int NT, int RB, bool TWO>
 __device__ __forceinline__ bool run_range(const Ring<RB>& ring, uint32_t lane_w, const uint32_t (&aoff)[NT],
-                                       uint32_t rslice, uint32_t rlane, int ipw, float (&acc)[RB][NT][4]) {
+                                          const uint32_t (&axor)[NT], uint32_t rslice, uint32_t rlane, int ipw,
+                                          float (&acc)[RB][NT][4]) {
     constexpr uint32_t kRec = FMT == kINT4 ? 96 : 512;
     int slot = 0;
     uint32_t ph = 0;
@@ -296,17 +358,28 @@ __device__ __forceinline__ bool run_range(const Ring<RB>& ring, uint32_t lane_w,
             return false;
         }
         // the step's activation fragments, read once for all its row blocks
+        // (unit c + 4j of the lane's row sits at 64 (j ^ parity) + 16 c)
         uint4 bv[NT][4];
 #pragma unroll
         for (int t = 0; t < NT; ++t)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) bv[t][j] = lds128(sb + aoff[t] + 64 * j);
+            for (int j = 0; j < 4; ++j) bv[t][j] = lds128(sb + aoff[t] + ((64u * j) ^ axor[t]));
+        if constexpr (FMT == kINT4) {
+            // row blocks in groups of two, each group's MMA chains
+            // interleaved; a CTA's row blocks past nb compute on stale slot
+            // bytes and are never stored
+            constexpr int QI = RB < 2 ? RB : 2;
 #pragma unroll
-        for (int q = 0; q < RB; ++q) {
-            if (q < ring.nb) {
-                const uint32_t rec = rslice + (uint32_t)(q * ipw + i) * kRec;
-                if constexpr (FMT == kINT4) step_int4<NT, TWO>(sb + 1024u * q + lane_w, rec, rlane, bv, acc[q]);
-                else step_fp4<NT, TWO>(sb + 1024u * q + lane_w, rec + rlane, bv, acc[q]);
+            for (int q0 = 0; q0 < RB; q0 += QI)
+                step_int4_group<NT, QI, TWO>(sb + 1024u * q0 + lane_w, rslice + (uint32_t)(q0 * ipw + i) * kRec,
+                                             (uint32_t)ipw * kRec, rlane, bv, &acc[q0]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < RB; ++q) {
+                if (q < ring.nb) {
+                    const uint32_t rec = rslice + (uint32_t)(q * ipw + i) * kRec;
+                    step_fp4<NT, TWO>(sb + 1024u * q + lane_w, rec + rlane, bv, acc[q]);
+                }
             }
         }
         slot_consumed<RB, NT>(acc);
@@ -323,7 +396,7 @@ __device__ __forceinline__ bool run_range(const Ring<RB>& ring, uint32_t lane_w,
 }
 
 template <int FMT, int NT, bool EPI, int RB>
-__global__ void __launch_bounds__(256, NT == 1 ? 3 : 2) gemv_pre_kernel(const PreArgs a) {
+__global__ void __launch_bounds__(256, 2) gemv_pre_kernel(const PreArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 127u) & ~127u;
     uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
@@ -356,7 +429,8 @@ __global__ void __launch_bounds__(256, NT == 1 ? 3 : 2) gemv_pre_kernel(const Pr
     ring.azero = a.A;
     ring.lda2 = 2 * (size_t)a.K;
     ring.krem = a.K - it0 * 128 - 8 * (lane & 15);
-    ring.adst = 1024u * RB + kAStride * (uint32_t)(lane >> 4) + 16u * (lane & 15);
+    // the lane's rows all have the parity of lane >> 4: one swizzled position
+    ring.adst = 1024u * RB + kAStride * (uint32_t)(lane >> 4) + 16u * ((lane & 15) ^ (4 * (lane >> 4)));
     ring.aunits = Mc > (lane >> 4) ? (Mc - (lane >> 4) + 1) >> 1 : 0;
     ring.nb = nb;
     ring.nit = nit;
@@ -462,17 +536,18 @@ __global__ void __launch_bounds__(256, NT == 1 ? 3 : 2) gemv_pre_kernel(const Pr
         // activation rows past Mc are not copied: those lanes read row 0 or 1
         // (keeping the row parity of a copied neighbour); their outputs are
         // never stored
-        uint32_t aoff[NT];
+        uint32_t aoff[NT], axor[NT];
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             const int m = t * 8 + r;
             const int ms = m < Mc ? m : (Mc > 1 ? (m & 1) : 0);
             aoff[t] = 1024u * RB + kAStride * (uint32_t)ms + 16u * c;
+            axor[t] = 64u * (uint32_t)(ms & 1);
         }
         const uint32_t lane_w = 32u * r + 16u * ((c >> 1) ^ ((r >> 2) & 1)) + 8u * (c & 1);
         const uint32_t rlane = kInt4 ? (uint32_t)r : (FMT == kNVFP4 ? (2u * r + (c >> 1)) * 32u : 32u * r);
-        ok = two ? run_range<FMT, NT, RB, true>(ring, lane_w, aoff, rslice, rlane, a.ipw, acc)
-                 : run_range<FMT, NT, RB, false>(ring, lane_w, aoff, rslice, rlane, a.ipw, acc);
+        ok = two ? run_range<FMT, NT, RB, true>(ring, lane_w, aoff, axor, rslice, rlane, a.ipw, acc)
+                 : run_range<FMT, NT, RB, false>(ring, lane_w, aoff, axor, rslice, rlane, a.ipw, acc);
     }
     if (!ok && lane == 0) record_pre_timeout();
     if (a.inputs_ready) grid_dependency_wait();   // completion order: stores after the predecessor's
@@ -610,18 +685,18 @@ bool choose_plan(int dev, int fmt, int NT, bool epi, int Mc, int mchunks, int Nb
     const int force_p = env_int("WQ_RING_P", 0);
     const double c_it = NT == 1 ? 140.0 : 170.0;   // issue cycles of one warp per 16 x 128 block
     if (ready && !force_rb && force_wk < 0 && force_p <= 0) {
-        // Measured on GB300 (chained int4 calls, N = 8192, K = 3072, M = 1, 4
-        // and 16; every (RB, Wk, P) in {1,2,4} x {1,2,4,8} x {2,3,4} tried):
-        // two-slot rings, two row blocks per CTA and ~512 warps per call are
-        // best or within 3 % of it at every M -- small CTAs of many calls
-        // keep the SMs' decode and the HBM stream busy together.  Take that
-        // shape when it fits (one row block per CTA when two would leave
-        // fewer CTAs than SMs), else fall through to the cost model.
-        const int RB = Nb >= 2 * sms ? 2 : 1;
+        // Measured on GB300 (chained int4 calls with their inputs ready, every
+        // (RB, Wk, P) in {1,2,4} x {1,2,4,8} x {2,3}, on the decoder's q/o,
+        // k/v, gate/up, down and LM-head shapes at M = 1, 4, 16): two-slot
+        // rings; up to 8 activation rows, four row blocks per CTA once there
+        // are 128 row blocks and ~256 warps per call; 16 rows, two row
+        // blocks and ~384 warps.  Within 5 % of the best shape everywhere.
+        // Take that shape when it fits, else fall through to the cost model.
+        const int RB = NT == 1 ? (Nb >= 128 ? 4 : (Nb >= 64 ? 2 : 1)) : (Nb >= 64 ? 2 : 1);
         const int G = (Nb + RB - 1) / RB;
-        const double want = 512.0 / ((double)G * mchunks);
+        const double want = (NT == 1 ? 256.0 : 384.0) / ((double)G * mchunks);
         int Wk = 1;
-        while (Wk < (1 << kMaxWkLog2) && Wk < want && 2 * Wk <= I) Wk *= 2;
+        while (Wk < (1 << kMaxWkLog2) && 2 * Wk <= want && 2 * Wk <= I) Wk *= 2;
         const KernFn kern = select_kernel(fmt, NT, RB, epi);
         if (!allow_smem(dev, kern)) return false;
         const Plan p = layout(RB, Wk, 2, Mc, I, fmt, MP);

@@ -195,53 +195,6 @@ __device__ __forceinline__ void slot_consumed(float (&acc)[RB][NT][4]) {
     __syncwarp();
 }
 
-// int4 g128, one row block of a step.  rec: its record block; the lane's
-// record pair {row r, row r + 8} (4 bytes each: bf16 scale | bf16 (128 +
-// min(z, 128)) << 16) sits at rec + 8 r, the pair of second subtrahends (2
-// bytes each, read only when some zero point exceeds 128) at rec + 64 + 4 r.
-template <int NT, bool TWO>
-__device__ __forceinline__ void step_int4(uint32_t wp, uint32_t rec, uint32_t r, const uint4 (&bv)[NT][4],
-                                          float (&acc)[NT][4]) {
-    uint4 qa, qb;
-    block_words(wp, qa, qb);
-    const uint2 rr = lds64(rec + 8u * r);
-    uint32_t zzA2 = 0, zzB2 = 0;
-    if constexpr (TWO) {
-        const uint32_t q = lds32(rec + 64u + 4u * r);
-        zzA2 = splat16(q);
-        zzB2 = splat16(q >> 16);
-    }
-    const uint32_t zzA = prmt(rr.x, rr.x, 0x3232u), zzB = prmt(rr.y, rr.y, 0x3232u);
-    const float sa = __uint_as_float(rr.x << 16), sb = __uint_as_float(rr.y << 16);
-    const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w}, wb[4] = {qb.x, qb.y, qb.z, qb.w};
-    // CH independent MMA chains per tile (words j = h mod CH): with one tile
-    // two chains keep the dependent sequence 4 deep; two tiles already are
-    // two chains
-    constexpr int CH = NT == 1 ? 2 : 1;
-    float part[CH][NT][4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint32_t pa[4], pb[4];
-        int4_word_kk4<TWO>(wa[j], zzA, zzA2, pa);
-        int4_word_kk4<TWO>(wb[j], zzB, zzB2, pb);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            if (j < CH) mma16816_z(part[j % CH][t], pa[0], pb[0], pa[1], pb[1], bv[t][j].x, bv[t][j].y);
-            else mma16816(part[j % CH][t], pa[0], pb[0], pa[1], pb[1], bv[t][j].x, bv[t][j].y);
-            mma16816(part[j % CH][t], pa[2], pb[2], pa[3], pb[3], bv[t][j].z, bv[t][j].w);
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float p = part[0][t][e];
-            if constexpr (CH == 2) p += part[CH - 1][t][e];
-            acc[t][e] = fmaf(e < 2 ? sa : sb, p, acc[t][e]);
-        }
-    }
-}
-
 // int4 g128, row blocks q0 .. q0 + QI - 1 of a step, their MMA chains
 // interleaved word by word (independent accumulators in flight together).
 // rec0: record block of row block 0 of this step; rec_stride: bytes between
@@ -270,8 +223,9 @@ __device__ __forceinline__ void step_int4_group(uint32_t wp0, uint32_t rec0, uin
             zzB2[q] = splat16(z2 >> 16);
         }
     }
-    // CH independent MMA chains per tile and row block (words j = h mod CH)
-    constexpr int CH = NT == 1 ? 2 : 1;
+    // one MMA chain per tile and row block: the QI row blocks' chains are
+    // already independent (a second chain per tile measured 1-2 % slower)
+    constexpr int CH = 1;
     float part[QI][CH][NT][4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {

@@ -104,7 +104,7 @@ def bench_config(workload: str, ws: int) -> dict:
 
 KERNEL_SOURCES = {  # files whose content defines the dominant kernel of a workload (and layout)
     "decode_int4": ["wq_gemv_tma.cu", "wq_gemv.cuh", "wq_common.cuh"],
-    "decode_int4:prepacked": ["wq_gemv_pre.cu", "wq_gemv.cuh", "wq_common.cuh"],
+    "decode_int4:prepacked": ["wq_gemv_pre.cu", "wq_gemv.cuh", "wq_common.cuh", "wq_tc.cuh"],
     "tiny_nvfp4": ["wq_gemv_tma.cu", "wq_gemv.cuh", "wq_common.cuh"],
     "tiny_nvfp4:prepacked": ["wq_gemv_pre.cu", "wq_gemv.cuh", "wq_common.cuh"],
     "prefill_mxfp4": ["wq_tc.cu", "wq_tc.cuh", "wq_common.cuh"],
@@ -707,7 +707,8 @@ def tensor_core_block(args, dev, gpu_id, peaks):
         tf = flops / (ms / 1e3) / 1e12
         out[name] = {"M": M, "N": N, "K": K, "format": fmt, "ms_per_call": ms, "tflops": tf, "calls": n_calls * reps,
                      "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                                  "frac": tf / peaks["bf16_tflops"],
+                                  "frac": tf / peaks["bf16_tflops"], "traffic": profiled_traffic(name + ":prepacked"),
+                                  "algorithmic_bytes_per_launch": metrics.call_bytes(fmt, M, N, K, group, "bf16"),
                                   "peak_source": peaks["source"] + " bf16_tflops (burst)"},
                      "clocks": clk, "layout": "prepacked", "rotation": f"{R} weight copies"}
         del g, pres, A, C, work

@@ -194,6 +194,34 @@ def test_side_stream_and_guard_region():
 
 
 # -- launch options -------------------------------------------------------------
+@pytest.mark.parametrize("fmt", ["int4", "nvfp4"])
+def test_inputs_ready_chain(fmt):
+    """WQ_LAUNCH_INPUTS_READY on the input layout: calls whose activations were
+    written before the chain read them at once and wait for their
+    predecessor only before storing; a dependent call and a plain stream
+    consumer afterwards see every output complete and oracle-green."""
+    N, K = 1024, 3072
+    dev = torch.device("cuda:0")
+    ps = [synth.make_problem(fmt, M, N, K, seed=60 + i) for i, M in enumerate((1, 4, 16, 2))]
+    ins = [to_dev(p) for p in ps]
+    torch.cuda.synchronize()
+    outs = [wq.gemm(A, pk, sc, zr, fmt, inputs_ready=True) for A, pk, sc, zr in ins]
+    q = synth.make_problem(fmt, 2, N, N, seed=69)
+    _, pk2, sc2, zr2 = to_dev(q)
+    torch.cuda.synchronize()
+    outs = [wq.gemm(A, pk, sc, zr, fmt, inputs_ready=True) for A, pk, sc, zr in ins]
+    y = wq.gemm(outs[-1], pk2, sc2, zr2, fmt, overlap=True)   # reads the last ready call's output
+    total = sum(o.float().sum() for o in outs)
+    torch.cuda.synchronize()
+    assert wq.wq_get_device_error() == wq.WQ_OK
+    for p, o in zip(ps, outs):
+        Ce, S = oracle_ref(p)
+        assert_parity(o.float().cpu().numpy().astype(np.float64), Ce, S, "bf16", f"{fmt} ready chain")
+    Ce, S = oracle_ref(dict(q, A=outs[-1].view(torch.int16).cpu().numpy().view(np.uint16)))
+    assert_parity(y.float().cpu().numpy().astype(np.float64), Ce, S, "bf16", f"{fmt} dependent after ready")
+    assert float(total) == float(sum(o.float().sum() for o in outs))
+
+
 def test_overlapped_launches_chain_correctly():
     """WQ_LAUNCH_OVERLAP: calls on one stream, each reading the previous
     call's output as its activations, must still see that output complete."""

@@ -121,7 +121,7 @@ __device__ __forceinline__ void block_words(uint32_t wp, uint4& qa, uint4& qb) {
 }
 
 // One warp's stream: step t (k-block it0 + t) lands in slot t mod P.
-template <int RB>
+template <int RB, int NT>
 struct Ring {
     uint32_t slots;           // slot 0 (shared address)
     uint32_t bar;             // barrier of slot 0 (8 bytes per slot)
@@ -134,6 +134,8 @@ struct Ring {
     int krem;                 // k left in the row from it0 * 128, minus 8 (lane & 15)
     uint32_t adst;            // the lane's first unit in a slot's activation rows
     int aunits;               // 16-byte units the lane copies per step: rows lane >> 4, + 2, ... < Mc
+    uint32_t lda2b;           // bytes between two activation rows
+    int kfull;                // steps that lie wholly inside K
     int nb, nit, P, lane;
 
     __device__ __forceinline__ void issue_codes(int t, int slot) const {
@@ -152,6 +154,18 @@ struct Ring {
     // lane's arrival on the slot's barrier, which covers every copy the lane
     // issued before it
     __device__ __forceinline__ void issue_acts(int t, int slot) const {
+        // two tiles, a step inside K, all 16 rows: the lane's 8 units at
+        // fixed offsets (v * 2 rows), no loop
+        if constexpr (NT == 2) {
+            if (t < kfull && aunits == 8) {
+                const uint32_t d = slots + slot_bytes * slot + adst;
+                const uint8_t* g = reinterpret_cast<const uint8_t*>(asrc + t * 128);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) cp_async16(d + 2u * kAStride * v, g + (uint32_t)v * lda2b);
+                cp_async_arrive_noinc(bar + 8u * slot);
+                return;
+            }
+        }
         uint32_t d = slots + slot_bytes * slot + adst;
         const bool in = t * 128 < krem;
         const uint16_t* g = in ? asrc + t * 128 : azero;
@@ -199,9 +213,20 @@ __device__ __forceinline__ void slot_consumed(float (&acc)[RB][NT][4]) {
 // interleaved word by word (independent accumulators in flight together).
 // rec0: record block of row block 0 of this step; rec_stride: bytes between
 // the record blocks of consecutive row blocks.
+// Activation fragments come from the slot (sa0): unit c + 4j of the lane's
+// row sits at aoffE + 64j for even j and aoffO + 64j for odd j (the row's
+// swizzle).  One tile (M <= 8) reads all four 32-k slices up front; two tiles
+// read each slice as its MMAs need it (the registers that holding all four
+// would take are what a 16-row step lacks).
 template <int NT, int QI, bool TWO>
 __device__ __forceinline__ void step_int4_group(uint32_t wp0, uint32_t rec0, uint32_t rec_stride, uint32_t r,
-                                                const uint4 (&bv)[NT][4], float (*acc)[NT][4]) {
+                                                uint32_t sa0, const uint32_t (&aoffE)[NT], const uint32_t (&aoffO)[NT],
+                                                float (*acc)[NT][4]) {
+    uint4 bv1[4];
+    if constexpr (NT == 1) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) bv1[j] = lds128(sa0 + ((j & 1) ? aoffO[0] : aoffE[0]) + 64u * j);
+    }
     uint32_t wa[QI][4], wb[QI][4], zzA[QI], zzB[QI], zzA2[QI], zzB2[QI];
     float sa[QI], sb[QI];
 #pragma unroll
@@ -229,6 +254,10 @@ __device__ __forceinline__ void step_int4_group(uint32_t wp0, uint32_t rec0, uin
     float part[QI][CH][NT][4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
+        uint4 bj[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+            bj[t] = NT == 1 ? bv1[j] : lds128(sa0 + ((j & 1) ? aoffO[t] : aoffE[t]) + 64u * j);
 #pragma unroll
         for (int q = 0; q < QI; ++q) {
             uint32_t pa[4], pb[4];
@@ -236,9 +265,9 @@ __device__ __forceinline__ void step_int4_group(uint32_t wp0, uint32_t rec0, uin
             int4_word_kk4<TWO>(wb[q][j], zzB[q], zzB2[q], pb);
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
-                if (j < CH) mma16816_z(part[q][j % CH][t], pa[0], pb[0], pa[1], pb[1], bv[t][j].x, bv[t][j].y);
-                else mma16816(part[q][j % CH][t], pa[0], pb[0], pa[1], pb[1], bv[t][j].x, bv[t][j].y);
-                mma16816(part[q][j % CH][t], pa[2], pb[2], pa[3], pb[3], bv[t][j].z, bv[t][j].w);
+                if (j < CH) mma16816_z(part[q][j % CH][t], pa[0], pb[0], pa[1], pb[1], bj[t].x, bj[t].y);
+                else mma16816(part[q][j % CH][t], pa[0], pb[0], pa[1], pb[1], bj[t].x, bj[t].y);
+                mma16816(part[q][j % CH][t], pa[2], pb[2], pa[3], pb[3], bj[t].z, bj[t].w);
             }
         }
     }
@@ -299,8 +328,8 @@ __device__ __forceinline__ void step_fp4(uint32_t wp, uint32_t rp, const uint4 (
 //   aoff   : the lane's activation offset in a slot, per MMA tile
 //   rlane  : the lane's offset in a record block (int4: its row r)
 template <int FMT, int NT, int RB, bool TWO>
-__device__ __forceinline__ bool run_range(const Ring<RB>& ring, uint32_t lane_w, const uint32_t (&aoff)[NT],
-                                          const uint32_t (&axor)[NT], uint32_t rslice, uint32_t rlane, int ipw,
+__device__ __forceinline__ bool run_range(const Ring<RB, NT>& ring, uint32_t lane_w, const uint32_t (&aoffE)[NT],
+                                          const uint32_t (&aoffO)[NT], uint32_t rslice, uint32_t rlane, int ipw,
                                           float (&acc)[RB][NT][4]) {
     constexpr uint32_t kRec = FMT == kINT4 ? 96 : 512;
     int slot = 0;
@@ -311,13 +340,6 @@ __device__ __forceinline__ bool run_range(const Ring<RB>& ring, uint32_t lane_w,
             ring.drain(i + 1, min(ring.nit, i + ring.P));
             return false;
         }
-        // the step's activation fragments, read once for all its row blocks
-        // (unit c + 4j of the lane's row sits at 64 (j ^ parity) + 16 c)
-        uint4 bv[NT][4];
-#pragma unroll
-        for (int t = 0; t < NT; ++t)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) bv[t][j] = lds128(sb + aoff[t] + ((64u * j) ^ axor[t]));
         if constexpr (FMT == kINT4) {
             // row blocks in groups of two, each group's MMA chains
             // interleaved; a CTA's row blocks past nb compute on stale slot
@@ -326,8 +348,14 @@ __device__ __forceinline__ bool run_range(const Ring<RB>& ring, uint32_t lane_w,
 #pragma unroll
             for (int q0 = 0; q0 < RB; q0 += QI)
                 step_int4_group<NT, QI, TWO>(sb + 1024u * q0 + lane_w, rslice + (uint32_t)(q0 * ipw + i) * kRec,
-                                             (uint32_t)ipw * kRec, rlane, bv, &acc[q0]);
+                                             (uint32_t)ipw * kRec, rlane, sb, aoffE, aoffO, &acc[q0]);
         } else {
+            // the step's activation fragments, read once for all its row blocks
+            uint4 bv[NT][4];
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) bv[t][j] = lds128(sb + ((j & 1) ? aoffO[t] : aoffE[t]) + 64u * j);
 #pragma unroll
             for (int q = 0; q < RB; ++q) {
                 if (q < ring.nb) {
@@ -373,7 +401,7 @@ __global__ void __launch_bounds__(256, 2) gemv_pre_kernel(const PreArgs a) {
     const int nit = max(0, min(a.I, it0 + a.ipw) - it0);   // this warp's k-blocks
     const uint32_t rslice = sbase + a.rec_off + (uint32_t)(warp * RB * a.ipw) * kRec;
 
-    Ring<RB> ring;
+    Ring<RB, NT> ring;
     ring.slots = sbase + a.ring_off + (uint32_t)(warp * a.P) * a.slot_bytes;
     ring.bar = sbase + 8u * (uint32_t)(warp * a.P);
     ring.slot_bytes = a.slot_bytes;
@@ -386,6 +414,8 @@ __global__ void __launch_bounds__(256, 2) gemv_pre_kernel(const PreArgs a) {
     // the lane's rows all have the parity of lane >> 4: one swizzled position
     ring.adst = 1024u * RB + kAStride * (uint32_t)(lane >> 4) + 16u * ((lane & 15) ^ (4 * (lane >> 4)));
     ring.aunits = Mc > (lane >> 4) ? (Mc - (lane >> 4) + 1) >> 1 : 0;
+    ring.lda2b = 4u * (uint32_t)a.K;
+    ring.kfull = a.K / 128 - it0;
     ring.nb = nb;
     ring.nit = nit;
     ring.P = a.P;
@@ -490,18 +520,21 @@ __global__ void __launch_bounds__(256, 2) gemv_pre_kernel(const PreArgs a) {
         // activation rows past Mc are not copied: those lanes read row 0 or 1
         // (keeping the row parity of a copied neighbour); their outputs are
         // never stored
-        uint32_t aoff[NT], axor[NT];
+        // (unit c + 4j of row ms sits at 16 c + 64 (j ^ (ms & 1)): +64 bytes
+        // for even j and -64 for odd j on odd rows)
+        uint32_t aoffE[NT], aoffO[NT];
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             const int m = t * 8 + r;
             const int ms = m < Mc ? m : (Mc > 1 ? (m & 1) : 0);
-            aoff[t] = 1024u * RB + kAStride * (uint32_t)ms + 16u * c;
-            axor[t] = 64u * (uint32_t)(ms & 1);
+            const uint32_t aoff = 1024u * RB + kAStride * (uint32_t)ms + 16u * c, sw = 64u * (uint32_t)(ms & 1);
+            aoffE[t] = aoff + sw;
+            aoffO[t] = aoff - sw;
         }
         const uint32_t lane_w = 32u * r + 16u * ((c >> 1) ^ ((r >> 2) & 1)) + 8u * (c & 1);
         const uint32_t rlane = kInt4 ? (uint32_t)r : (FMT == kNVFP4 ? (2u * r + (c >> 1)) * 32u : 32u * r);
-        ok = two ? run_range<FMT, NT, RB, true>(ring, lane_w, aoff, axor, rslice, rlane, a.ipw, acc)
-                 : run_range<FMT, NT, RB, false>(ring, lane_w, aoff, axor, rslice, rlane, a.ipw, acc);
+        ok = two ? run_range<FMT, NT, RB, true>(ring, lane_w, aoffE, aoffO, rslice, rlane, a.ipw, acc)
+                 : run_range<FMT, NT, RB, false>(ring, lane_w, aoffE, aoffO, rslice, rlane, a.ipw, acc);
     }
     if (!ok && lane == 0) record_pre_timeout();
     if (a.inputs_ready) grid_dependency_wait();   // completion order: stores after the predecessor's

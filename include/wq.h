@@ -111,6 +111,13 @@ int wq_gemm(const void* A, const uint8_t* packed, const void* scales, const uint
  * an explicit kernel choice (WQ_PATH_*, optionally | WQ_LAUNCH_OVERLAP).
  * WQ_PATH_TC returns WQ_ERR_UNSUPPORTED for shapes that kernel does not take
  * (K not a multiple of 64, or row strides not 16-byte aligned for TMA).
+ * Where the tensor-core path has so few tiles (128 weight rows x up to 256
+ * activation rows) that each can take two or more SMs, it runs each tile on
+ * one thread-block cluster of up to 8 CTAs that split the tile's k-steps
+ * evenly and add their fp32 partial sums through distributed shared memory,
+ * in cluster-rank order (deterministic; no workspace; the method itself has
+ * no such step -- it computes the same sum of products).  WQ_TC_CSK in the
+ * environment: 0 turns this off, S >= 2 asks for S CTAs per tile (tests).
  */
 int wq_gemm_ex(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
                void* C, int M, int N, int K, int format, int group, void* stream, int path);
@@ -190,8 +197,9 @@ int wq_gemm_fused(const void* A, const uint8_t* packed, const void* scales, cons
                   void* workspace, size_t workspace_bytes, void* stream, int path);
 
 /* Workspace bytes wq_gemm_ws can use for this shape on the current device
- * (0: the shape needs none -- M <= 16, tiles that fill whole waves, or an
- * invalid description). */
+ * (0: the shape needs none -- M <= 16, tiles that fill whole waves, tiles
+ * split over thread-block clusters (wq_gemm_ex), or an invalid
+ * description). */
 size_t wq_gemm_workspace_size(int M, int N, int K, int format, int group);
 
 /* The same size under the name the library's design gives it (an alias of

@@ -83,7 +83,8 @@ def test_gate_up_decode_shape():
 
 
 @pytest.mark.parametrize("M", [128, 300])
-def test_stream_k_owner_applies_the_epilogue(M):
+def test_stream_k_owner_applies_the_epilogue(M, monkeypatch):
+    monkeypatch.setenv("WQ_TC_CSK", "0")   # stream-K, not the cluster split of these few tiles
     p = synth.make_problem("int4", M, 512, 4096, seed=M + 5)
     ws = wq.workspace(M, 512, 4096, "int4")
     assert ws is not None

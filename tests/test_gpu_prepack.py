@@ -369,9 +369,10 @@ def test_tc_parity(fmt, N, K, M):
 
 
 @pytest.mark.parametrize("fmt", ["int4", "nvfp4", "mxfp4"])
-def test_tc_streamk_workspace(fmt):
+def test_tc_streamk_workspace(fmt, monkeypatch):
     """A shape whose whole tiles fill the SMs badly runs split (stream-K) with a
     workspace; same parity, and the workspace's flag words are left zero."""
+    monkeypatch.setenv("WQ_TC_CSK", "0")   # stream-K, not the cluster split of these few tiles
     M, N, K = 128, 3072, 3072
     p = synth.make_problem(fmt, M, N, K, seed=5)
     ws = wq.workspace(M, N, K, fmt, p["group"], torch.device("cuda:0"))

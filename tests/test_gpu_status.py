@@ -36,6 +36,7 @@ def test_streamk_flag_wait_runs_out(monkeypatch):
     workspace must be zeroed again; then the same call is oracle-green."""
     from gpu_util import assert_parity, oracle_ref, to_dev
     M, N, K = 128, 1024, 3072            # 8 tiles on the SMs: split over many CTAs
+    monkeypatch.setenv("WQ_TC_CSK", "0")   # by stream-K (the cluster split needs no flags)
     p = synth.make_problem("int4", M, N, K, seed=5)
     n = wq.wq_gemm_workspace_size(M, N, K, wq.WQ_INT4, 128)
     assert n > 0

@@ -15,6 +15,13 @@ from gpu_util import check_full, check_sampled, gpu_gemm, to_dev
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True)
+def streamk_not_clusters(monkeypatch):
+    """These shapes have few tiles, which the library would otherwise split
+    over thread-block clusters (tests/test_gpu_cluster.py) instead."""
+    monkeypatch.setenv("WQ_TC_CSK", "0")
+
+
 def ws_for(p):
     n = wq.wq_gemm_workspace_size(p["M"], p["N"], p["K"], wq.FORMATS[p["fmt"]], p["group"])
     return torch.zeros(max(n, 256), dtype=torch.uint8, device="cuda"), n

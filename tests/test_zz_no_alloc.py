@@ -17,6 +17,13 @@ from gpu_util import assert_parity, oracle_ref, to_dev
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True)
+def streamk_not_clusters(monkeypatch):
+    """The split shapes have few tiles, which the library would otherwise split
+    over thread-block clusters (tests/test_gpu_cluster.py) instead."""
+    monkeypatch.setenv("WQ_TC_CSK", "0")
+
+
 def run_static(p, out="fp32", path=wq.WQ_PATH_AUTO):
     A, packed, scales, zeros = to_dev(p)
     odt = torch.float32 if out == "fp32" else torch.bfloat16
@@ -124,3 +131,17 @@ def test_static_gemv_path_ignores_the_scratch_cap(monkeypatch):
     assert st == wq.WQ_OK
     Ce, S = oracle_ref(p)
     assert_parity(C, Ce, S, "fp32", "static, GEMV path, no scratch")
+
+
+def test_static_cluster_split_needs_no_scratch(monkeypatch):
+    """Few tiles split over thread-block clusters add their partial sums on
+    chip: the call uses no scratch, so even a zero usable scratch serves it."""
+    monkeypatch.setenv("WQ_TC_CSK", "1")
+    monkeypatch.setenv("WQ_STATIC_WS_CAP", "0")
+    p = synth.make_problem("int4", 128, 3072, 3072, seed=8)
+    assert wq.wq_gemm_workspace_size(128, 3072, 3072, wq.WQ_INT4, 128) == 0
+    st, C = run_static(p)
+    assert st == wq.WQ_OK
+    assert wq.wq_get_device_error() == wq.WQ_OK
+    Ce, S = oracle_ref(p)
+    assert_parity(C, Ce, S, "fp32", "static, cluster split-K")

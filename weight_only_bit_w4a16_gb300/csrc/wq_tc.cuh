@@ -257,6 +257,41 @@ __device__ __forceinline__ void tmem_st2_32x32b_x32_sync(uint32_t taddr0, const 
 }
 
 // ---------------------------------------------------------------------------
+// thread-block cluster: barrier and distributed shared memory
+// ---------------------------------------------------------------------------
+// Every thread of every CTA of the cluster arrives (release: its earlier
+// shared-memory writes become visible to the cluster) and waits (acquire).
+// A hardware barrier, not a polled one: it completes once all the cluster's
+// threads have arrived, so every path through a kernel that uses it must
+// reach it.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// the shared::cluster address of this CTA's shared-memory address `addr` in
+// the CTA of cluster rank `rank`
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// ---------------------------------------------------------------------------
 // descriptors
 // ---------------------------------------------------------------------------
 // Shared-memory matrix descriptor of a K-major operand tile stored with the

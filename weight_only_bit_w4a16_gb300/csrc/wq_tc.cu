@@ -525,9 +525,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 for (int k = kb; k < ke; ++k, ++g) {
                     const int s = g % kStages, b = g % kWBufs;
-                    const uint32_t ph = (g / kStages) & 1, phb = (g / kWBufs) & 1;
-                    if (!mbar_wait_bounded(smem_u32(&sh.full[s]), ph, abort, kWaitNs) ||
-                        !mbar_wait_bounded(smem_u32(&sh.wfull[b]), phb, abort, kWaitNs)) {
+                    const uint32_t phb = (g / kWBufs) & 1;
+                    // One wait, for the decoded weights: the decode set waited
+                    // for this k-step's stage copy (full[s]) before decoding and
+                    // arrived on wfull[b] after, so the copy is ordered before
+                    // this acquire through its arrivals.  This thread is the
+                    // pipeline's critical path -- a satisfied mbarrier wait costs
+                    // it ~120 cycles, against ~590 of MMA in a k-step -- and
+                    // dropping the second wait measured (same GPU): MXFP4
+                    // 2048 x 3072^2 32.1 -> 30.4 us, int4 128 x 128256 x 3072
+                    // 187 -> 176 us, 8192^3 NVFP4 761 -> 748 us.
+                    if (!mbar_wait_bounded(smem_u32(&sh.wfull[b]), phb, abort, kWaitNs)) {
                         record_timeout();
                         ok = false;
                         break;

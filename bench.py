@@ -653,6 +653,10 @@ def tensor_core_block(args, dev, gpu_id, peaks):
     l2 = getattr(props, "L2_cache_size", 128 * 1024 * 1024)
     s = torch.cuda.Stream(dev)
     out = {}
+    # the calls chained as the decode line's are (--launch); the tensor-core
+    # kernel takes programmatic dependent launch for launches of up to two
+    # waves of tiles
+    launch_flags = LAUNCH_FLAGS[args.launch](wq)
 
     def timed(g_, n_calls, reps):
         g_.replay()
@@ -692,7 +696,8 @@ def tensor_core_block(args, dev, gpu_id, peaks):
         with torch.cuda.stream(s):
             def go(i, h):
                 st = wq.wq_gemm_prepacked(A.data_ptr(), pres[i % R].buf.data_ptr(), C.data_ptr(), M, N, K,
-                                          wq.FORMATS[fmt], group, None, work.data_ptr(), wsb, h, wq.WQ_PATH_AUTO)
+                                          wq.FORMATS[fmt], group, None, work.data_ptr(), wsb, h,
+                                          wq.WQ_PATH_AUTO | launch_flags)
                 if st != wq.WQ_OK:
                     raise wq.WQError(st, name)
             go(0, s.cuda_stream)
@@ -710,7 +715,8 @@ def tensor_core_block(args, dev, gpu_id, peaks):
                                   "frac": tf / peaks["bf16_tflops"], "traffic": profiled_traffic(name + ":prepacked"),
                                   "algorithmic_bytes_per_launch": metrics.call_bytes(fmt, M, N, K, group, "bf16"),
                                   "peak_source": peaks["source"] + " bf16_tflops (burst)"},
-                     "clocks": clk, "layout": "prepacked", "rotation": f"{R} weight copies"}
+                     "clocks": clk, "layout": "prepacked", "rotation": f"{R} weight copies",
+                     "launch": LAUNCH_DESC[args.launch] + " (tensor-core kernel: up to two waves of tiles)"}
         del g, pres, A, C, work
         torch.cuda.synchronize()
         torch.cuda.empty_cache()

@@ -73,7 +73,10 @@ extern "C" {
 /* OR into `path`: launch with programmatic dependent launch, so that the
  * GEMV kernel starts streaming its weights while the preceding kernel on the
  * stream is still running (A is read and C written only after that kernel
- * has completed).  The caller guarantees that the preceding kernel does not
+ * has completed).  The tensor-core kernel takes it for launches of up to two
+ * waves of tiles and for split tiles: it sets up (tensor memory, barriers)
+ * while its predecessor finishes, and reads A and writes C, partial sums and
+ * flags only after that predecessor has completed.  The caller guarantees that the preceding kernel does not
  * write packed, scales, zeros or the prepacked buffer -- true whenever they
  * are model weights, and false right after the wq_prepack that writes them
  * (synchronise first). */
@@ -87,7 +90,7 @@ extern "C" {
  * (projections that share one input, independent weights of one step)
  * overlaps end to end while still completing in stream order: a later
  * operation on the stream sees the results of every earlier call.  The
- * tensor-core path ignores the bit. */
+ * tensor-core path treats the bit as WQ_LAUNCH_OVERLAP. */
 #define WQ_LAUNCH_INPUTS_READY 0x200
 
 /* status codes */

@@ -70,10 +70,10 @@ int gemm_impl(const void* A, const uint8_t* packed, const void* scales, const ui
 
     if (path == WQ_PATH_TC)
         return wq::launch_tc(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, workspace, workspace_bytes,
-                             epi, s);
+                             epi, overlap, s);
     if (path == WQ_PATH_AUTO && M > 16 && K > 0) {
         st = wq::launch_tc(A, packed, scales, zeros, C, M, N, K, fmt, group, out_f32, workspace, workspace_bytes,
-                           epi, s);
+                           epi, overlap, s);
         if (st != WQ_ERR_UNSUPPORTED) return st;
         // shapes the tensor-core kernel does not take run on the GEMV kernel
     }
@@ -204,10 +204,10 @@ WQ_EXPORT int wq_gemm_prepacked(const void* A, const void* prepacked, void* C, i
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (route == WQ_PATH_TC)
         return wq::launch_tc_prepacked(A, prepacked, C, M, N, K, fmt, group, out_f32, workspace, workspace_bytes,
-                                       epi, s);
+                                       epi, overlap, s);
     if (route == WQ_PATH_AUTO && M > 16) {
         const int st = wq::launch_tc_prepacked(A, prepacked, C, M, N, K, fmt, group, out_f32, workspace,
-                                               workspace_bytes, epi, s);
+                                               workspace_bytes, epi, overlap, s);
         if (st != WQ_ERR_UNSUPPORTED) return st;
     }
     return wq::launch_gemv_prepacked(A, prepacked, C, M, N, K, fmt, out_f32, overlap, inputs_ready, epi, s);

@@ -11,6 +11,7 @@
 #pragma once
 
 #include "wq_common.cuh"
+#include "wq_tc.cuh"
 
 namespace wq {
 namespace gemv {
@@ -32,11 +33,10 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 // different bank groups.
 __device__ __forceinline__ int a_unit(int u, int m) { return u ^ ((((u >> 3) & 1) << 1) | (m & 1)); }
 
-// programmatic dependent launch: no-ops when the grid was launched without it
-__device__ __forceinline__ void grid_dependents_launch() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// defined with the tensor-core primitives (wq_tc.cuh)
+using sm100::fence_proxy_async_smem;
+using sm100::grid_dependency_wait;
+using sm100::grid_dependents_launch;
 
 __device__ __forceinline__ uint4 lds128(uint32_t saddr) {
     uint4 v;
@@ -63,8 +63,6 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
-
-// (fence_proxy_async_smem is defined in wq_tc.cuh)
 
 __device__ __forceinline__ void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

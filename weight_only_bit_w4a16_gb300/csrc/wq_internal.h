@@ -34,16 +34,18 @@ int launch_gemv_tma(const void* A, const uint8_t* packed, const void* scales, co
 // kernel does not take.  With a workspace of at least tc_workspace_bytes()
 // (zero-initialised before its first use; every completed call leaves it
 // zero) the kernel may split tiles across CTAs (stream-K); without one each
-// CTA computes whole tiles.
+// CTA computes whole tiles.  pdl: launched with programmatic dependent
+// launch -- the grid may start while its predecessor on the stream runs, and
+// reads A, and writes C, only after the predecessor has completed.
 int launch_tc(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros,
               void* C, int M, int N, int K, int fmt, int group, bool out_f32, void* workspace,
-              size_t workspace_bytes, const Epilogue& epi, cudaStream_t stream);
+              size_t workspace_bytes, const Epilogue& epi, bool pdl, cudaStream_t stream);
 size_t tc_workspace_bytes(int M, int N, int K, int fmt);
 
 // The tensor-core kernel on prepacked weights (same contract as launch_tc;
 // one k-step of 128 rows is 8 row blocks' half blocks).
 int launch_tc_prepacked(const void* A, const void* prepacked, void* C, int M, int N, int K, int fmt, int group,
-                        bool out_f32, void* workspace, size_t workspace_bytes, const Epilogue& epi,
+                        bool out_f32, void* workspace, size_t workspace_bytes, const Epilogue& epi, bool pdl,
                         cudaStream_t stream);
 
 // The prepacked layout (include/wq.h, above wq_prepack_bytes): its size,

@@ -115,6 +115,7 @@ struct TcArgs {
     int G;              // CTAs of a stream-K launch
     int csk;            // cluster split-K: CTAs per tile, one thread-block cluster (0: not this mode)
     int tma_store;      // whole tiles, plain bf16 C: staged in shared memory at scr_off, bulk tensor store (tmapC)
+    int pdl;            // launched with programmatic dependent launch
     int kblocks;        // prepacked weights: 128-k blocks per row
     int vec_store;      // C rows 16-byte aligned and the store scratch allocated: vector stores of C
     int scr_off;        // byte offset of the decode warps' store scratch (2 KB each) in shared memory
@@ -485,17 +486,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
+    // Programmatic dependent launch (no-ops otherwise).  This grid reads A
+    // only after its predecessor has completed (the producer's wait below),
+    // and every write it makes to global memory -- C, stream-K partials and
+    // flags, the bulk stores -- follows from copies the producer issued after
+    // that wait.  The next grid may be scheduled once every CTA has begun its
+    // last segment (the producer's trigger below): at once in a one-wave
+    // launch, late in a longer one.
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             prefetch_tensormap(&tmapA);
             prefetch_tensormap(&tmapP);
+            if (a.pdl) grid_dependency_wait();
             int g = 0;   // k-steps issued so far (the stage ring runs across segments)
             bool ok = true;
             int tile, kb, ke;
             for (int i = 0; ok && get_seg(a, cta, i, tile, kb, ke); ++i) {
                 const int n0 = (tile % a.nt_n) * kBN, m0 = (tile / a.nt_n) * a.bm;
+                if (a.pdl) {
+                    int t2, kb2, ke2;
+                    if (!get_seg(a, cta, i + 1, t2, kb2, ke2)) grid_dependents_launch();   // the last segment
+                }
                 for (int k = kb; k < ke; ++k, ++g) {
                     const int s = g % kStages;
                     const uint32_t ph = (g / kStages) & 1;
@@ -880,20 +893,29 @@ int launch_fmt(const CUtensorMap& ta, const CUtensorMap& tp, const TcArgs& args,
     }
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return WQ_ERR_CUDA;
-    if (args.csk) {
-        // one cluster of csk CTAs per tile
+    if (args.csk || args.pdl) {
+        // one cluster of csk CTAs per tile; programmatic dependent launch
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
         cfg.blockDim = dim3(kThreads, 1, 1);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)args.csk;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
+        cudaLaunchAttribute attr[2];
+        unsigned na = 0;
+        if (args.csk) {
+            attr[na].id = cudaLaunchAttributeClusterDimension;
+            attr[na].val.clusterDim.x = (unsigned)args.csk;
+            attr[na].val.clusterDim.y = 1;
+            attr[na].val.clusterDim.z = 1;
+            ++na;
+        }
+        if (args.pdl) {
+            attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[na].val.programmaticStreamSerializationAllowed = 1;
+            ++na;
+        }
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = na;
         return cudaLaunchKernelEx(&cfg, kern, ta, tp, args, tcm) == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
     }
     kern<<<grid, kThreads, smem, stream>>>(ta, tp, args, tcm);
@@ -1201,7 +1223,7 @@ namespace {
 // scale arrays or the record blocks.
 int run_tc(const void* A, const CUtensorMap& tp, bool pre, const uint8_t* scales, const uint8_t* zeros,
            int kblocks, void* C, int M, int N, int K, int fmt, int group, bool out_f32, void* workspace,
-           size_t workspace_bytes, const Epilogue& epi, cudaStream_t stream) {
+           size_t workspace_bytes, const Epilogue& epi, bool pdl, cudaStream_t stream) {
     const int sms = device_sms();
     TcPlan plan = plan_tc(M, N, K, sms, workspace != nullptr, fmt);
     if (plan.streamk && workspace_bytes < plan.ws_bytes) plan = plan_tc(M, N, K, sms, false, fmt);
@@ -1251,6 +1273,14 @@ int run_tc(const void* A, const CUtensorMap& tp, bool pre, const uint8_t* scales
     args.units = plan.units;
     args.G = plan.G;
     args.csk = plan.csk;
+    // Programmatic dependent launch for launches of up to two waves (and
+    // every split plan): same GPU, MXFP4 2048 x 3072^2 29.5 -> 28.6 us, int4
+    // 128 x 1024 x 3072 10.7 -> 9.7 us, 128 x 3072^2 12.7 -> 11.8 us.  A
+    // longer persistent launch gained nothing and lost up to 2 % (8192^3
+    // NVFP4, 13.5 tiles per CTA: the dependent CTAs land on SMs in the
+    // order the predecessor frees them, not the placement whole-tile
+    // scheduling relies on for sharing activation tiles in L2).
+    args.pdl = (pdl && (plan.streamk || plan.csk || plan.tiles <= 2LL * plan.G)) ? 1 : 0;
     args.kblocks = kblocks;
     args.flag_wait_ns = kWaitNs;
     if (const char* e = getenv("WQ_TC_FLAG_WAIT_NS")) args.flag_wait_ns = strtoull(e, nullptr, 10);   // tests
@@ -1301,7 +1331,7 @@ int run_tc(const void* A, const CUtensorMap& tp, bool pre, const uint8_t* scales
 
 int launch_tc(const void* A, const uint8_t* packed, const void* scales, const uint8_t* zeros, void* C, int M,
               int N, int K, int fmt, int group, bool out_f32, void* workspace, size_t workspace_bytes,
-              const Epilogue& epi, cudaStream_t stream) {
+              const Epilogue& epi, bool pdl, cudaStream_t stream) {
     if (M == 0 || N == 0) return WQ_OK;
     // shapes this kernel takes: whole k-steps, TMA-legal strides, aligned
     // scale rows for the per-k-step scale loads
@@ -1313,11 +1343,11 @@ int launch_tc(const void* A, const uint8_t* packed, const void* scales, const ui
                    kBK / 2, kBN, CU_TENSOR_MAP_SWIZZLE_32B))
         return WQ_ERR_UNSUPPORTED;
     return run_tc(A, tp, false, static_cast<const uint8_t*>(scales), zeros, 0, C, M, N, K, fmt, group, out_f32,
-                  workspace, workspace_bytes, epi, stream);
+                  workspace, workspace_bytes, epi, pdl, stream);
 }
 
 int launch_tc_prepacked(const void* A, const void* prepacked, void* C, int M, int N, int K, int fmt, int group,
-                        bool out_f32, void* workspace, size_t workspace_bytes, const Epilogue& epi,
+                        bool out_f32, void* workspace, size_t workspace_bytes, const Epilogue& epi, bool pdl,
                         cudaStream_t stream) {
     if (M == 0 || N == 0) return WQ_OK;
     if (K <= 0 || K % kBK != 0) return WQ_ERR_UNSUPPORTED;
@@ -1333,7 +1363,7 @@ int launch_tc_prepacked(const void* A, const void* prepacked, void* C, int M, in
     if (!encode_3d(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT32, prepacked, dims, strides, box)) return WQ_ERR_UNSUPPORTED;
     const uint8_t* recs = static_cast<const uint8_t*>(prepacked) + Nb * I * 1024;
     return run_tc(A, tp, true, recs, nullptr, (int)I, C, M, N, K, fmt, group, out_f32, workspace, workspace_bytes,
-                  epi, stream);
+                  epi, pdl, stream);
 }
 
 }  // namespace wq

@@ -616,79 +616,113 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
         constexpr int D = 4;                    // this set's k-steps of scales in flight
         constexpr int KS = kDecodeSets;
+        // Decode k-step gg (running count) from its scale keys into weight
+        // buffer gg mod kWBufs; false once a wait gave up (decided per warp:
+        // the TMEM store is warp-collective).
+        auto decode_kstep = [&](int gg, const GroupKey (&key)[4]) -> bool {
+            const int s = gg % kStages, b = gg % kWBufs;
+            const uint32_t ph = (gg / kStages) & 1, phb = (gg / kWBufs) & 1;
+            // Weight buffer first, stage second.  A set never waits on
+            // the stage phase of k-step gg - kStages (another set's), so
+            // on its own the parity test on full[s] could match that
+            // older phase when copies land out of order, and the decode
+            // would read the stage before this k-step's copy.  The MMA
+            // of k-step gg - kWBufs has consumed every copy up to it,
+            // that of gg - kStages included, so the full[s] wait after
+            // it can only match this k-step's phase.
+            static_assert(kWBufs == kStages,
+                          "weight buffer b is freed by the commit that frees stage b; the "
+                          "weight-buffer wait must imply the older stage phase");
+            const bool got = mbar_wait_bounded(smem_u32(&sh.empty[b]), phb ^ 1, abort, kWaitNs) &&
+                             mbar_wait_bounded(smem_u32(&sh.full[s]), ph, abort, kWaitNs);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (!got) record_timeout();
+                return false;
+            }
+            tc_fence_after();
+            // this row's 32 packed bytes; 32-byte swizzle: chunk c of row r
+            // sits at 32 r + 16 (c ^ ((r >> 2) & 1))
+            const uint8_t* prow = smem + s * kStageBytes + kATileBytes + row * 32;
+            const int x = (row >> 2) & 1;
+            const uint4 lo = *reinterpret_cast<const uint4*>(prow + 16 * x);
+            const uint4 hi = *reinterpret_cast<const uint4*>(prow + 16 * (x ^ 1));
+            uint32_t w[32], w2[32];
+            bool two = false;
+            if constexpr (FMT != kNVFP4) two = __any_sync(0xffffffffu, key[0].two || key[1].two);
+            if constexpr (PRE) {
+                if (two) decode_row_pre<FMT, true>(lo, hi, key, w, w2);
+                else decode_row_pre<FMT, false>(lo, hi, key, w, w2);
+            } else {
+                if (two) decode_row<FMT, true>(lo, hi, key, w, w2);
+                else decode_row<FMT, false>(lo, hi, key, w, w2);
+            }
+            const uint32_t wbuf = lane_base + kAccColsOf<FMT> + b * kWColsOf<FMT>;
+            if constexpr (FMT == kINT4)
+                tmem_st2_32x32b_x32_sync(wbuf, w, wbuf + 32, w2);
+            else
+                tmem_st_32x32b_x32_sync(wbuf, w);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&sh.wfull[b]));
+            return true;
+        };
+        auto raw_of = [&](int nrow, int k) -> uint2 {
+            return PRE ? tc_raw_pre<FMT>(a, nrow, k) : tc_raw<FMT>(a, nrow, k);
+        };
+        auto keys_of = [&](const uint2& r, GroupKey (&key)[4]) {
+            if constexpr (PRE) tc_keys_pre<FMT>(r, key);
+            else tc_keys<FMT>(r, key);
+        };
         int g = 0;
         bool ok = true;
+        bool ahead = false;   // this set's first k-step of the segment was decoded during the previous one
         int tile, kb, ke;
         for (int i = 0; get_seg(a, cta, i, tile, kb, ke); ++i) {
             const int n0 = (tile % a.nt_n) * kBN, m0 = (tile / a.nt_n) * a.bm;
             const int n = n0 + row;
             const int nc = n < a.N ? n : a.N - 1;   // rows past N decode row N-1 (never stored)
             const int g0 = g;
-            const int k1 = kb + ((dset - g0) % KS + KS) % KS;  // this set's first k-step of the segment
+            // this set's first k-step of the segment still to decode
+            const int k1 = kb + ((dset - g0) % KS + KS) % KS + (ahead ? KS : 0);
             uint2 raw[D];
 #pragma unroll
             for (int d = 0; d < D; ++d)
-                if (k1 + d * KS < ke) raw[d] = PRE ? tc_raw_pre<FMT>(a, nc, k1 + d * KS) : tc_raw<FMT>(a, nc, k1 + d * KS);
+                if (k1 + d * KS < ke) raw[d] = raw_of(nc, k1 + d * KS);
             for (int kk0 = k1; kk0 < ke && ok; kk0 += D * KS) {
 #pragma unroll
                 for (int d = 0; d < D; ++d) {
                     const int k = kk0 + d * KS;
                     if (k < ke && ok) {
-                        const int gg = g0 + (k - kb);
-                        const int s = gg % kStages, b = gg % kWBufs;
-                        const uint32_t ph = (gg / kStages) & 1, phb = (gg / kWBufs) & 1;
                         GroupKey key[4];
-                        if constexpr (PRE) tc_keys_pre<FMT>(raw[d], key);
-                        else tc_keys<FMT>(raw[d], key);
-                        if (k + D * KS < ke)
-                            raw[d] = PRE ? tc_raw_pre<FMT>(a, nc, k + D * KS) : tc_raw<FMT>(a, nc, k + D * KS);
-                        // Weight buffer first, stage second.  A set never waits on
-                        // the stage phase of k-step gg - kStages (another set's), so
-                        // on its own the parity test on full[s] could match that
-                        // older phase when copies land out of order, and the decode
-                        // would read the stage before this k-step's copy.  The MMA
-                        // of k-step gg - kWBufs has consumed every copy up to it,
-                        // that of gg - kStages included, so the full[s] wait after
-                        // it can only match this k-step's phase.
-                        static_assert(kWBufs == kStages,
-                                      "weight buffer b is freed by the commit that frees stage b; the "
-                                      "weight-buffer wait must imply the older stage phase");
-                        const bool got = mbar_wait_bounded(smem_u32(&sh.empty[b]), phb ^ 1, abort, kWaitNs) &&
-                                         mbar_wait_bounded(smem_u32(&sh.full[s]), ph, abort, kWaitNs);
-                        // the tcgen05.st below is warp-collective: decide as a warp
-                        if (!__all_sync(0xffffffffu, got)) {
-                            if (!got) record_timeout();
+                        keys_of(raw[d], key);
+                        if (k + D * KS < ke) raw[d] = raw_of(nc, k + D * KS);
+                        if (!decode_kstep(g0 + (k - kb), key)) {
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
-                        // this row's 32 packed bytes; 32-byte swizzle: chunk c of row r
-                        // sits at 32 r + 16 (c ^ ((r >> 2) & 1))
-                        const uint8_t* prow = smem + s * kStageBytes + kATileBytes + row * 32;
-                        const int x = (row >> 2) & 1;
-                        const uint4 lo = *reinterpret_cast<const uint4*>(prow + 16 * x);
-                        const uint4 hi = *reinterpret_cast<const uint4*>(prow + 16 * (x ^ 1));
-                        uint32_t w[32], w2[32];
-                        bool two = false;
-                        if constexpr (FMT != kNVFP4) two = __any_sync(0xffffffffu, key[0].two || key[1].two);
-                        if constexpr (PRE) {
-                            if (two) decode_row_pre<FMT, true>(lo, hi, key, w, w2);
-                            else decode_row_pre<FMT, false>(lo, hi, key, w, w2);
-                        } else {
-                            if (two) decode_row<FMT, true>(lo, hi, key, w, w2);
-                            else decode_row<FMT, false>(lo, hi, key, w, w2);
-                        }
-                        const uint32_t wbuf = lane_base + kAccColsOf<FMT> + b * kWColsOf<FMT>;
-                        if constexpr (FMT == kINT4)
-                            tmem_st2_32x32b_x32_sync(wbuf, w, wbuf + 32, w2);
-                        else
-                            tmem_st_32x32b_x32_sync(wbuf, w);
-                        tc_fence_before();
-                        mbar_arrive(smem_u32(&sh.wfull[b]));
                     }
                 }
             }
             g = g0 + (ke - kb);
+            // Look-ahead: this set's first k-step of the next segment, decoded
+            // before this segment's epilogue.  Its weight buffer is freed by
+            // MMAs of this segment, not by the epilogue, so the issuer finds
+            // the next tile's first weights ready once the accumulator is
+            // released (per-k-step stamps: the issuer had waited ~4,500 cycles
+            // for them at every tile boundary of int4 2048 x 128256 x 3072).
+            ahead = false;
+            {
+                int tile2, kb2, ke2;
+                if (ok && get_seg(a, cta, i + 1, tile2, kb2, ke2)) {
+                    const int k1n = kb2 + ((dset - g) % KS + KS) % KS;
+                    if (k1n < ke2) {
+                        const int n2 = (tile2 % a.nt_n) * kBN + row;
+                        GroupKey key2[4];
+                        keys_of(raw_of(n2 < a.N ? n2 : a.N - 1, k1n), key2);
+                        ok = decode_kstep(g + (k1n - kb2), key2);
+                        ahead = true;
+                    }
+                }
+            }
 
             // ---------------- epilogue of the segment ----------------
             // (cluster split-K: no CTA owns its tile; all add up on chip later)

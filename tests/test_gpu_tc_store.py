@@ -64,10 +64,34 @@ def test_thread_store_shapes(out, N, stores):
     assert stores() == "threads"
 
 
-def test_prefill_workload_bulk_store(stores):
-    """The prefill workload at full size keeps its two-MMA tiles of 352 rows
-    (above 256: thread stores); 2048 x 3072 x 3072 int4 at 256 rows stores
-    in bulk."""
+def test_int4_2048_bulk_store(stores):
+    """int4 2048 x 3072 x 3072: tiles of at most 256 rows, staged beside the
+    stage ring."""
     p = synth.make_problem("int4", 2048, 3072, 3072, seed=11)
     check_sampled(p, "bf16", k=16, path="tc", what="int4 2048x3072x3072 bulk store")
     assert stores() == "bulk tensor"
+
+
+def test_prefill_two_mma_tiles_stage_over_the_ring(stores, monkeypatch):
+    """The prefill workload (MXFP4 2048 x 3072 x 3072): 144 tiles of 352
+    rows, one per CTA, too tall to stage beside the ring, so they stage over
+    it once their MMAs are done and leave as two boxes of 176 rows; same
+    bits as the decode warps' stores."""
+    p = synth.workload_problem("prefill_mxfp4")
+    C1 = gpu_gemm_dev(p, "bf16", path="tc")
+    assert stores() == "bulk tensor"
+    monkeypatch.setenv("WQ_TC_NO_TMA_STORE", "1")
+    C2 = gpu_gemm_dev(p, "bf16", path="tc")
+    assert stores() == "threads"
+    assert torch.equal(C1, C2)
+    monkeypatch.delenv("WQ_TC_NO_TMA_STORE")
+    check_sampled(p, "bf16", k=16, path="tc", what="prefill bulk store over the ring")
+
+
+def test_two_mma_tiles_several_per_cta_keep_thread_stores(stores, monkeypatch):
+    """Tiles of 352 rows with more tiles than SMs: a CTA's ring serves its
+    next tile, so these keep the decode warps' stores."""
+    monkeypatch.setenv("WQ_TC_BM", "352")
+    p = synth.make_problem("nvfp4", 2816, 2560, 512, seed=13)   # 8 x 20 = 160 tiles > SMs
+    check_sampled(p, "bf16", k=16, path="tc", what="352-row tiles, several per CTA")
+    assert stores() == "threads"

@@ -114,7 +114,8 @@ struct TcArgs {
     long long units;    // tiles * nks
     int G;              // CTAs of a stream-K launch
     int csk;            // cluster split-K: CTAs per tile, one thread-block cluster (0: not this mode)
-    int tma_store;      // whole tiles, plain bf16 C: staged in shared memory at scr_off, bulk tensor store (tmapC)
+    int tma_store;      // whole tiles, plain bf16 C: staged in shared memory at stg_off, bulk tensor store (tmapC)
+    int stg_off;        // the staging tile: beside the stage ring, or over it when each CTA has one tile
     int pdl;            // launched with programmatic dependent launch
     int kblocks;        // prepacked weights: 128-k blocks per row
     int vec_store;      // C rows 16-byte aligned and the store scratch allocated: vector stores of C
@@ -743,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 asm volatile("bar.sync 1, %0;" ::"n"(kDecodeSets * 128) : "memory");
                 if (!ok && lane == 0) record_timeout();
                 tc_fence_after();
-                __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(smem + a.scr_off);
+                __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(smem + a.stg_off);
 #pragma unroll 1
                 for (int ch = dset; ch < a.bm / 32 && ok; ch += kDecodeSets) {
                     uint32_t v[32];
@@ -756,7 +757,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 asm volatile("bar.sync 1, %0;" ::"n"(kDecodeSets * 128) : "memory");
                 if (warp == 2 && lane == 0 && ok) {
+                    // boxes of bh rows: two for a two-MMA tile
                     tma_store_2d(&tmapC, smem_u32(stg), n0, m0);
+                    if (a.bh < a.bm) tma_store_2d(&tmapC, smem_u32(stg) + (uint32_t)a.bh * kBN * 2, n0, m0 + a.bh);
                     bulk_commit();
                 }
                 continue;
@@ -1350,12 +1353,20 @@ int run_tc(const void* A, const CUtensorMap& tp, bool pre, const uint8_t* scales
     CUtensorMap tcm;
     memset(&tcm, 0, sizeof(tcm));
     const bool any_epi = epi.bias || epi.residual || epi.gated;
-    args.tma_store = !any_epi && !out_f32 && !plan.streamk && !plan.csk && bm <= kBMMax && N % 8 == 0 &&
-                     (reinterpret_cast<uintptr_t>(C) & 15) == 0 && 1024 + (size_t)args.scr_off + (size_t)bm * 256 <= kMaxDynSmem &&
-                     !getenv("WQ_TC_NO_TMA_STORE") &&
-                     encode_2d(&tcm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, kBN, bm,
+    // The staging tile (bm x 128 bf16) sits beside the stage ring where it
+    // fits; a tile of more than 256 rows (two-MMA fp4) stages over the ring
+    // itself when every CTA has one tile: its ring is idle once its MMAs
+    // have completed, and no later tile's copies come (same GPU, MXFP4
+    // 2048 x 3072^2, 144 tiles of 352 rows: 29.5 -> 28.6 us).
+    const bool one_tile_per_cta = !plan.streamk && !plan.csk && plan.tiles <= plan.G;
+    const bool beside = 1024 + (size_t)args.scr_off + (size_t)bm * 256 <= kMaxDynSmem;
+    const bool over = bm > kBMMax && one_tile_per_cta && (size_t)kStages * args.stage_bytes >= (size_t)bm * 256;
+    args.stg_off = beside ? args.scr_off : 0;
+    args.tma_store = !any_epi && !out_f32 && !plan.streamk && !plan.csk && (beside || over) && N % 8 == 0 &&
+                     (reinterpret_cast<uintptr_t>(C) & 15) == 0 && !getenv("WQ_TC_NO_TMA_STORE") &&
+                     encode_2d(&tcm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, kBN, bh,
                                CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (args.tma_store) smem = 1024 + (size_t)args.scr_off + (size_t)bm * 256;
+    if (args.tma_store && beside) smem = 1024 + (size_t)args.scr_off + (size_t)bm * 256;
     if (debug_on()) fprintf(stderr, "wq: tensor-core C stores: %s\n", args.tma_store ? "bulk tensor" : "threads");
     switch (fmt) {
         case kNVFP4:

@@ -169,3 +169,30 @@ def test_workspace_size_alias():
     """wq_workspace_bytes is wq_gemm_workspace_size under its design name."""
     for args in ((300, 3072, 3072, 2, 128), (4, 512, 1024, 2, 128), (0, 8, 64, 0, 16), (300, 1000, 1024, 1, 32)):
         assert wq.wq_workspace_bytes(*args) == wq.wq_gemm_workspace_size(*args)
+
+
+def test_cluster_split_plans_need_no_workspace(monkeypatch):
+    """Host planning (no GPU needed: the planner assumes an SM count without
+    a device).  128 x 3072 x 3072 has 24 tiles of 128 weight rows: too few
+    to fill the SMs, so each runs on a thread-block cluster whose CTAs add
+    their partial sums on chip -- no workspace.  With the cluster mode off
+    the same shape asks for stream-K's workspace, and a forced cluster size
+    whose CTAs would not fit on the SMs falls back to stream-K as well."""
+    shape = (128, 3072, 3072, wq.WQ_INT4, 128)
+    monkeypatch.delenv("WQ_TC_CSK", raising=False)
+    assert wq.wq_gemm_workspace_size(*shape) == 0
+    monkeypatch.setenv("WQ_TC_CSK", "0")
+    assert wq.wq_gemm_workspace_size(*shape) > 0
+    monkeypatch.setenv("WQ_TC_CSK", "8")          # 24 tiles x 8 CTAs: more than the SMs
+    assert wq.wq_gemm_workspace_size(*shape) > 0
+    monkeypatch.setenv("WQ_TC_CSK", "2")          # 48 CTAs fit
+    assert wq.wq_gemm_workspace_size(*shape) == 0
+
+
+def test_full_waves_need_no_workspace_either_way(monkeypatch):
+    """Shapes whose whole tiles fill the SMs' waves run whole tiles: no
+    workspace with or without the cluster mode."""
+    for setting in ("1", "0"):
+        monkeypatch.setenv("WQ_TC_CSK", setting)
+        assert wq.wq_gemm_workspace_size(8192, 8192, 8192, wq.WQ_NVFP4, 16) == 0
+        assert wq.wq_gemm_workspace_size(2048, 128256, 3072, wq.WQ_INT4, 128) == 0

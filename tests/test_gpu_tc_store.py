@@ -41,11 +41,13 @@ def test_ragged_bulk_store(fmt, M, N, K, stores):
     assert stores() == "bulk tensor"
 
 
-@pytest.mark.parametrize("fmt,M,N,K", [("int4", 300, 1000, 1024), ("nvfp4", 2048, 3072, 3072)])
-def test_same_bits_as_thread_stores(fmt, M, N, K, stores, monkeypatch):
-    # tiles of 256 rows (the NVFP4 shape would take two-MMA tiles of 352
-    # rows, which keep the thread stores)
-    monkeypatch.setenv("WQ_TC_BM", "256")
+@pytest.mark.parametrize("fmt,M,N,K,bm", [("int4", 300, 1000, 1024, 256), ("nvfp4", 2048, 3072, 3072, 128)])
+def test_same_bits_as_thread_stores(fmt, M, N, K, bm, stores, monkeypatch):
+    # Forced tile heights with room for the staging tile beside the ring: the
+    # NVFP4 shape would take two-MMA tiles of 352 rows (thread stores, several
+    # tiles per CTA), and its one-MMA tiles of 256 rows fill shared memory
+    # with their six stages.
+    monkeypatch.setenv("WQ_TC_BM", str(bm))
     p = synth.make_problem(fmt, M, N, K, seed=7)
     C1 = gpu_gemm_dev(p, "bf16", path="tc")
     assert stores() == "bulk tensor"

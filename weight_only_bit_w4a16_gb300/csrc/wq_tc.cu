@@ -79,16 +79,29 @@ constexpr int kBN = 128;        // weight rows per tile (MMA M)
 constexpr int kBMMax = 256;     // activation rows of one MMA (its N), of an int4 tile and of a stream-K tile
 constexpr int kBMMaxFp4 = 384;  // activation rows of an fp4 data-parallel tile: two MMAs of N = bm / 2
 constexpr int kBK = 64;         // k per stage
-constexpr int kStages = 4;
-constexpr int kWBufs = 4;       // TMEM weight buffers
+// Stages of the ring, and TMEM weight buffers (as many: stage s and weight
+// buffer s are freed by one commit).  A k-step's copy is issued when the MMAs
+// kStages k-steps back complete, and it must land (~1,500 cycles) and be
+// decoded (~600) before its own MMAs: with 4 stages that chain, not the
+// tensor pipe, set the k-step of one-MMA fp4 tiles (~700 cycles against
+// ~512 of MMA at 256 rows).  Their 32-column weight buffers leave TMEM room
+// for 6 beside a 256-column accumulator (same GPU, bit-identical: 8192^3
+// NVFP4 724 -> 654 (5 stages) -> 626 us; 128 x 8192 x 3072 17.2 -> 15.6
+// us).  int4 (64-column buffers) and the two-MMA fp4 tiles (a 384-column
+// accumulator) keep 4.
+constexpr int kStagesMax = 6;
+template <int FMT, bool SPLIT>
+constexpr int kStagesOf = (FMT != kINT4 && !SPLIT) ? 6 : 4;
 constexpr int kTmemCols = 512;
 // TMEM columns per weight buffer (bf16 pairs of a row's 64 weights: int4 hi
 // then lo, fp4 the weights alone) and the fp32 accumulator's columns before them
 template <int FMT>
 constexpr int kWColsOf = FMT == kINT4 ? 2 * kBK / 2 : kBK / 2;
-template <int FMT>
-constexpr int kAccColsOf = kTmemCols - kWBufs * kWColsOf<FMT>;
-static_assert(kAccColsOf<kINT4> >= kBMMax && kAccColsOf<kNVFP4> >= kBMMaxFp4, "TMEM budget");
+template <int FMT, bool SPLIT>
+constexpr int kAccColsOf = kTmemCols - kStagesOf<FMT, SPLIT> * kWColsOf<FMT>;
+static_assert(kAccColsOf<kINT4, false> >= kBMMax && kAccColsOf<kNVFP4, false> >= kBMMax &&
+                  kAccColsOf<kNVFP4, true> >= kBMMaxFp4,
+              "TMEM budget");
 constexpr int kDecodeSets = 3;                      // decode warp sets, taking the k-steps in turn
 constexpr int kThreads = 64 + kDecodeSets * 128;    // producer, MMA, decode/epilogue warps
 constexpr int kPTileBytes = kBN * kBK / 2;          // 4 KB of packed weights per stage
@@ -125,9 +138,9 @@ struct TcArgs {
 };
 
 struct __align__(8) TcShared {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t wfull[kWBufs];
+    uint64_t full[kStagesMax];
+    uint64_t empty[kStagesMax];
+    uint64_t wfull[kStagesMax];
     uint64_t accfull;
     uint64_t accempty;
     uint64_t drain;
@@ -463,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap tmapA, const __grid_constant__ CUtensorMap tmapP, const TcArgs a,
               const __grid_constant__ CUtensorMap tmapC) {
     static_assert(!(SPLIT && FMT == kINT4), "int4 tiles use one MMA per slice and its residual");
+    constexpr int kStages = kStagesOf<FMT, SPLIT>, kWBufs = kStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // stages 1024-byte aligned (the 128-byte swizzle pattern repeats every 1 KB)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -579,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a_addr = smem_u32(smem + s * kStageBytes);
                     const uint64_t bdesc0 = smem_desc_sw128_kmajor(a_addr);
                     const uint64_t bdesc1 = SPLIT ? smem_desc_sw128_kmajor(a_addr + a.bh * 128) : 0;
-                    const uint32_t wcol0 = tmem + kAccColsOf<FMT> + b * kWColsOf<FMT>;
+                    const uint32_t wcol0 = tmem + kAccColsOf<FMT, SPLIT> + b * kWColsOf<FMT>;
                     const uint32_t acc0 = k != kb ? 1u : 0u;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
@@ -657,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (two) decode_row<FMT, true>(lo, hi, key, w, w2);
                 else decode_row<FMT, false>(lo, hi, key, w, w2);
             }
-            const uint32_t wbuf = lane_base + kAccColsOf<FMT> + b * kWColsOf<FMT>;
+            const uint32_t wbuf = lane_base + kAccColsOf<FMT, SPLIT> + b * kWColsOf<FMT>;
             if constexpr (FMT == kINT4)
                 tmem_st2_32x32b_x32_sync(wbuf, w, wbuf + 32, w2);
             else
@@ -1275,7 +1289,8 @@ int run_tc(const void* A, const CUtensorMap& tp, bool pre, const uint8_t* scales
     if (plan.streamk && workspace_bytes < plan.ws_bytes) plan = plan_tc(M, N, K, sms, false, fmt);
     if (plan.csk) {
         // every tile's cluster resident at once, else fewer CTAs per tile
-        const size_t smem_c = 1024 + (size_t)kStages * (plan.bm * kBK * 2 + kPTileBytes) + sizeof(TcShared);
+        const int st_c = fmt == kINT4 ? kStagesOf<kINT4, false> : kStagesOf<kNVFP4, false>;
+        const size_t smem_c = 1024 + (size_t)st_c * (plan.bm * kBK * 2 + kPTileBytes) + sizeof(TcShared);
         while (plan.csk >= 2 && csk_max_clusters(plan.csk, smem_c) < plan.tiles) --plan.csk;
         if (plan.csk >= 2) {
             plan.G = plan.tiles * plan.csk;
@@ -1335,7 +1350,9 @@ int run_tc(const void* A, const CUtensorMap& tp, bool pre, const uint8_t* scales
         fprintf(stderr, "wq: tcgen05%s M=%d N=%d K=%d: bm=%d tiles=%d %s grid=%d\n", pre ? " (prepacked)" : "", M, N,
                 K, bm, plan.tiles, plan.csk ? "cluster split-K" : plan.streamk ? "stream-K" : "data-parallel", plan.G);
     const dim3 grid(plan.G, 1, 1);
-    size_t smem = 1024 + (size_t)kStages * args.stage_bytes + sizeof(TcShared);
+    const int nst = fmt == kINT4 ? kStagesOf<kINT4, false>
+                    : (bh < bm ? kStagesOf<kNVFP4, true> : kStagesOf<kNVFP4, false>);
+    size_t smem = 1024 + (size_t)nst * args.stage_bytes + sizeof(TcShared);
     // Stream-K launches stage C through the decode warps' store scratch (2 KB
     // each) and write it in 16-byte pieces, where the output rows are 16-byte
     // aligned: there the owner's stores are on the critical path (same GPU:
@@ -1344,7 +1361,7 @@ int run_tc(const void* A, const CUtensorMap& tp, bool pre, const uint8_t* scales
     // tiles' work (with the scratch: 8192^3 NVFP4 778 -> 782 us).
     constexpr size_t kScrBytes = (size_t)kDecodeSets * 4 * 2048;
     constexpr size_t kMaxDynSmem = 227 * 1024;
-    args.scr_off = (int)(((size_t)kStages * args.stage_bytes + sizeof(TcShared) + 255) / 256 * 256);
+    args.scr_off = (int)(((size_t)nst * args.stage_bytes + sizeof(TcShared) + 255) / 256 * 256);
     args.vec_store = plan.streamk && (N % (out_f32 ? 4 : 8) == 0) &&
                      1024 + (size_t)args.scr_off + kScrBytes <= kMaxDynSmem;
     if (args.vec_store) smem = 1024 + (size_t)args.scr_off + kScrBytes;
@@ -1360,7 +1377,7 @@ int run_tc(const void* A, const CUtensorMap& tp, bool pre, const uint8_t* scales
     // 2048 x 3072^2, 144 tiles of 352 rows: 29.5 -> 28.6 us).
     const bool one_tile_per_cta = !plan.streamk && !plan.csk && plan.tiles <= plan.G;
     const bool beside = 1024 + (size_t)args.scr_off + (size_t)bm * 256 <= kMaxDynSmem;
-    const bool over = bm > kBMMax && one_tile_per_cta && (size_t)kStages * args.stage_bytes >= (size_t)bm * 256;
+    const bool over = bm > kBMMax && one_tile_per_cta && (size_t)nst * args.stage_bytes >= (size_t)bm * 256;
     args.stg_off = beside ? args.scr_off : 0;
     args.tma_store = !any_epi && !out_f32 && !plan.streamk && !plan.csk && (beside || over) && N % 8 == 0 &&
                      (reinterpret_cast<uintptr_t>(C) & 15) == 0 && !getenv("WQ_TC_NO_TMA_STORE") &&

@@ -1114,24 +1114,25 @@ int device_sms() {
     return sms;
 }
 
-// Cycles of one k-step of an fp4 data-parallel tile of bm rows, measured on
-// the prepacked layout (8192^3 NVFP4 and 2048 x 3072^2 MXFP4, 2070 MHz): one
-// MMA is decode-bound at ~896 cycles up to 256 rows (its own time, ~2.6 per
-// row, stays below that); two MMAs on one decode cost ~3.67 per row (1180 at
-// 320 rows, ~1290 at 352).
-long long fp4_kstep_cycles(int bm) {
-    return bm <= kBMMax ? (896 > 26 * bm / 10 ? 896 : 26 * bm / 10) : 367LL * bm / 100;
-}
+// Cycles of an fp4 data-parallel tile of bm rows: a fixed ~10,200 per tile
+// (the first copies and decode, the accumulator's readout) and per k-step
+// ~450 + 0.75 bm for one MMA (six stages; the copy and decode chain, not
+// the MMA's ~2 cycles per row, sets it), ~2.8 per row for two (four
+// stages).  Fitted to forced tile heights on the prepacked layout at 2070
+// MHz: NVFP4 8192^3 and 2048 x 8192 x 3072, 4096^3, MXFP4 4096 x 3072^2,
+// 2048 x 3072^2 and 1024 x 3072^2, tiles of 128..352 rows.
+constexpr long long kFp4TileCycles = 10200;
+long long fp4_kstep_cycles(int bm) { return bm <= kBMMax ? 450 + 3LL * bm / 4 : 28LL * bm / 10; }
 
 // Tile height (activation rows) for M rows.  Data-parallel: least time, the
-// waves of one-CTA-per-SM tiles times a tile's k-step cost -- for int4 about
-// (bm + 64) (MMA time grows with bm, the decode of a k-step does not), for
-// the fp4 formats fp4_kstep_cycles, up to 384 rows (two MMAs on one decode,
-// chosen where they save enough waves: the 2048 x 3072 x 3072 prefill runs 144
-// tiles of 352 rows in one wave instead of 264 of 192 in two).  Stream-K:
-// least total work, tiles x (bm + 64), as the CTAs share it evenly, up to 256
-// rows.
-int choose_bm(int M, int N, int sms, bool streamk, int fmt) {
+// waves of one-CTA-per-SM tiles times a tile's cost -- for int4 about
+// (bm + 64) per k-step (MMA time grows with bm, the decode of a k-step does
+// not), for the fp4 formats kFp4TileCycles + nks fp4_kstep_cycles, up to
+// 384 rows (two MMAs on one decode, chosen where they save enough waves:
+// the 2048 x 3072 x 3072 prefill runs 144 tiles of 352 rows in one wave
+// instead of 264 of 192 in two).  Stream-K: least total work, tiles x
+// (bm + 64), as the CTAs share it evenly, up to 256 rows.
+int choose_bm(int M, int N, int nks, int sms, bool streamk, int fmt) {
     const int nt = (N + kBN - 1) / kBN;
     const int bm_max = (fmt != kINT4 && !streamk) ? kBMMaxFp4 : kBMMax;
     int bm = 0;
@@ -1142,12 +1143,12 @@ int choose_bm(int M, int N, int sms, bool streamk, int fmt) {
         const long long waves = (tiles + sms - 1) / sms;
         const long long cost = streamk ? tiles * (cand + 64)
                                : fmt == kINT4 ? waves * (cand + 64)
-                                              : waves * fp4_kstep_cycles(cand);
-        // candidates run from tall to short.  On a tie of the fp4 model (the
-        // same waves of decode-bound one-MMA tiles) the shorter tile wins: the
-        // same time, fewer padded rows.  The int4 and stream-K models keep the
-        // taller tile (2048 x 8192 x 3072 int4: 4 waves of 256 rows run 122 us,
-        // 5 of 192 rows 142 us, which the (bm + 64) model scores alike).
+                                              : waves * (kFp4TileCycles + nks * fp4_kstep_cycles(cand));
+        // candidates run from tall to short.  On a tie of the fp4 model the
+        // shorter tile wins (fewer padded rows).  The int4 and stream-K models
+        // keep the taller tile (2048 x 8192 x 3072 int4: 4 waves of 256 rows
+        // run 122 us, 5 of 192 rows 142 us, which the (bm + 64) model scores
+        // alike).
         const bool fp4_dp = fmt != kINT4 && !streamk;
         if (best < 0 || cost < best || (fp4_dp && cost == best)) {
             best = cost;
@@ -1190,7 +1191,7 @@ TcPlan plan_tc(int M, int N, int K, int sms, bool allow_streamk, int fmt, bool a
     // out, partials in) costs more than the idle SMs (measured: 2048 x 3072 x
     // 3072 runs 87% full on whole tiles and is faster that way; 128 x 3072 x
     // 3072 -- 24 tiles on 152 SMs -- runs 1.8x faster split)
-    int bm = choose_bm(M, N, sms, false, fmt);
+    int bm = choose_bm(M, N, p.nks, sms, false, fmt);
     long long tiles = (long long)p.nt_n * ((M + bm - 1) / bm);
     const long long waves = (tiles + sms - 1) / sms;
     const bool thin = (double)tiles / (double)(waves * sms) < 0.75;
@@ -1203,7 +1204,7 @@ TcPlan plan_tc(int M, int N, int K, int sms, bool allow_streamk, int fmt, bool a
     p.csk = 0;
     const int csk_mode = csk_setting();
     if (allow_csk && thin && csk_mode != 0 && !(getenv("WQ_TC_STREAMK") && sk)) {
-        const int bmc = choose_bm(M, N, sms, true, fmt);
+        const int bmc = choose_bm(M, N, p.nks, sms, true, fmt);
         const long long tc = (long long)p.nt_n * ((M + bmc - 1) / bmc);
         long long S = csk_mode >= 2 ? csk_mode : sms / tc;
         if (S > 8) S = 8;

@@ -205,5 +205,57 @@ __device__ __forceinline__ void it_int4(const uint4& qa, const uint4& qb, const 
     }
 }
 
+// two outputs rounded to bf16 (RNE), the first in the low half
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// The final stores of a small-M CTA, plain output in 16-byte pieces: 8 bf16
+// or 4 fp32 outputs per thread and pass.  red holds the Wk warps' partial
+// sums, [warp][MP activation rows][ld] floats with the CTA's 2^outs_log2
+// weight rows contiguous (ld a multiple of 4, the rows 16-byte aligned);
+// each output sums them in warp order from 0, as the scalar stores do, so
+// both give the same bits.  C must be 16-byte aligned and N a multiple of 8
+// (bf16) or 4 (fp32); n0 and n_end are then multiples of a piece.
+// These stores run after the preceding call has completed and before this
+// one can, so on a chain of calls they are on its critical path: a 16-row
+// ring call's scalar 2-byte stores took ~2.4 us there (per-CTA stamps).
+template <int MP>
+__device__ __forceinline__ void store_pieces(const float* red, int ld, int Wk, int Mc, int outs_log2, int n0,
+                                             int n_end, int mz, int N, void* C, bool out_f32, int tid, int nthreads) {
+    const int vl2 = out_f32 ? 2 : 3;       // log2 outputs per piece
+    const int pl2 = outs_log2 - vl2;       // log2 pieces per activation row
+    for (int i = tid; i < (Mc << pl2); i += nthreads) {
+        const int m = i >> pl2, rl = (i & ((1 << pl2) - 1)) << vl2;
+        const int n = n0 + rl;
+        if (n >= n_end) continue;
+        const float* src = red + (size_t)m * ld + rl;
+        float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+        for (int q = 0; q < Wk; ++q) {
+            const float4 x0 = *reinterpret_cast<const float4*>(src + (size_t)q * MP * ld);
+            v0.x += x0.x;
+            v0.y += x0.y;
+            v0.z += x0.z;
+            v0.w += x0.w;
+            if (!out_f32) {
+                const float4 x1 = *reinterpret_cast<const float4*>(src + (size_t)q * MP * ld + 4);
+                v1.x += x1.x;
+                v1.y += x1.y;
+                v1.z += x1.z;
+                v1.w += x1.w;
+            }
+        }
+        const size_t o = (size_t)(mz + m) * N + n;
+        if (out_f32) {
+            *reinterpret_cast<float4*>(static_cast<float*>(C) + o) = v0;
+        } else {
+            const uint4 w = make_uint4(bf16x2_bits(v0.x, v0.y), bf16x2_bits(v0.z, v0.w), bf16x2_bits(v1.x, v1.y),
+                                       bf16x2_bits(v1.z, v1.w));
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(C) + o) = w;
+        }
+    }
+}
+
 }  // namespace gemv
 }  // namespace wq

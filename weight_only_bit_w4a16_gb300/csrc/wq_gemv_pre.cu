@@ -89,6 +89,7 @@ struct PreArgs {
     uint32_t ring_off, rec_off;
     int wide;               // grid x Nb does not fit 32 bits
     int inputs_ready;       // A may be read before the preceding kernel completes
+    int vec_store;          // plain output in 16-byte pieces: C 16-byte aligned, N a multiple of 8 (bf16) or 4 (fp32)
     Epilogue epi;
 };
 
@@ -563,6 +564,12 @@ __global__ void __launch_bounds__(256, 2) gemv_pre_kernel(const PreArgs a) {
     constexpr int outs_full = rows;
     const int outs = gated ? outs_full >> 1 : outs_full;   // a power of two
     const int outs_log2 = 31 - __clz(outs);
+    if constexpr (!EPI) {
+        if (a.vec_store) {
+            store_pieces<MP>(red, ld, Wk, Mc, outs_log2, n0, n_end, mz, a.N, a.C, a.out_f32, tid, blockDim.x);
+            return;
+        }
+    }
     for (int i = tid; i < Mc * outs; i += blockDim.x) {
         const int m = i >> outs_log2, o = i & (outs - 1);
         const int rl = gated ? (((o >> 3) << 4) | (o & 7)) : o;
@@ -822,6 +829,7 @@ int launch_gemv_prepacked(const void* A, const void* prepacked, void* C, int M, 
     args.rec_off = plan.rec_off;
     args.wide = (unsigned long long)(plan.grid + 1) * (unsigned long long)Nb >= (1ull << 32) ? 1 : 0;
     args.inputs_ready = inputs_ready ? 1 : 0;
+    args.vec_store = (reinterpret_cast<uintptr_t>(C) & 15) == 0 && N % (out_f32 ? 4 : 8) == 0 && !getenv("WQ_GEMV_SCALAR_STORE");
     args.epi = epi;
 
     cudaLaunchConfig_t cfg = {};

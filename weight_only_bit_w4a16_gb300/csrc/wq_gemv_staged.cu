@@ -71,6 +71,7 @@ struct PreArgs {
     uint32_t SA;            // shared row stride of the activations (bytes)
     uint32_t w_off, a_off, r_off, red_off;
     int inputs_ready;       // A may be read before the preceding kernel completes
+    int vec_store;          // plain output in 16-byte pieces: C 16-byte aligned, N a multiple of 8 (bf16) or 4 (fp32)
     Epilogue epi;
 };
 
@@ -341,6 +342,12 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_staged_kernel(const
     const bool gated = EPI && a.epi.gated;
     const int outs = gated ? rows >> 1 : rows;   // a power of two
     const int outs_log2 = 31 - __clz(outs);
+    if constexpr (!EPI) {
+        if (a.vec_store) {
+            store_pieces<MP>(red, ld, Wk, Mc, outs_log2, n0, n_end, mz, a.N, a.C, a.out_f32, tid, blockDim.x);
+            return;
+        }
+    }
     for (int i = tid; i < Mc * outs; i += blockDim.x) {
         const int m = i >> outs_log2, o = i & (outs - 1);
         const int rl = gated ? (((o >> 3) << 4) | (o & 7)) : o;
@@ -556,6 +563,7 @@ int launch_gemv_staged(const void* A, const void* prepacked, void* C, int M, int
     args.r_off = plan.r_off;
     args.red_off = plan.red_off;
     args.inputs_ready = inputs_ready ? 1 : 0;
+    args.vec_store = (reinterpret_cast<uintptr_t>(C) & 15) == 0 && N % (out_f32 ? 4 : 8) == 0 && !getenv("WQ_GEMV_SCALAR_STORE");
     args.epi = epi;
 
     cudaLaunchConfig_t cfg = {};

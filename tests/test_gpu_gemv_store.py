@@ -64,3 +64,34 @@ def test_unaligned_rows_keep_single_stores(kernel, out, N, monkeypatch):
     C2 = run(p, out, ready, monkeypatch, scalar=True)
     assert torch.equal(C1, C2)
     assert_parity(C1.float().cpu().numpy().astype(np.float64), Ce, S, out, f"{kernel} {out} N={N}")
+
+
+def test_ready_calls_into_one_output_keep_stream_order(monkeypatch):
+    """Calls with their inputs declared ready compute before the preceding
+    call completes and store after it: consecutive calls into the same C
+    leave the last call's result, and a plain consumer between them sees
+    the earlier one."""
+    monkeypatch.delenv("WQ_GEMV_SCALAR_STORE", raising=False)
+    monkeypatch.setenv("WQ_GEMV_PRE_KERNEL", "ring")
+    N, K = 2048, 3072
+    ps = [synth.make_problem("int4", M, N, K, seed=90 + i) for i, M in enumerate((16, 16, 16, 16))]
+    pres = []
+    for p in ps:
+        _, packed, scales, zeros = to_dev(p)
+        pres.append(wq.prepack(packed, scales, zeros, p["fmt"], p["group"]))
+    A = to_dev(ps[0])[0]
+    torch.cuda.synchronize()
+    C = torch.empty((16, N), dtype=torch.bfloat16, device="cuda")
+    snaps = []
+    for rep in range(3):
+        for i, pre in enumerate(pres):
+            wq.gemm_prepacked(A, pre, out=C, inputs_ready=True)
+            if i == 1:
+                snaps.append(C.clone())   # a plain stream consumer after the second call
+    torch.cuda.synchronize()
+    assert wq.wq_get_device_error() == wq.WQ_OK
+    A_bits = ps[0]["A"]
+    for idx, got in ((3, C), (1, snaps[-1])):
+        Ce, S = oracle_ref(dict(ps[idx], A=A_bits))
+        assert_parity(got.float().cpu().numpy().astype(np.float64), Ce, S, "bf16", f"call {idx} into a shared C")
+    assert all(torch.equal(snaps[0], s) for s in snaps[1:])

@@ -1,4 +1,4 @@
-"""The small-M prepacked kernels' final stores: plain output in 16-byte pieces
+"""The small-M kernels' final stores: plain output in 16-byte pieces
 where C is 16-byte aligned and N a multiple of 8 (bf16) or 4 (fp32), else
 one output per thread.  Parity against the oracle, and the same bits as the
 one-output stores (WQ_GEMV_SCALAR_STORE), on both kernels (the ring kernel
@@ -12,7 +12,7 @@ import torch
 import weight_only_bit_w4a16_gb300 as wq
 from weight_only_bit_w4a16_gb300 import synth
 
-from gpu_util import assert_parity, oracle_ref, to_dev
+from gpu_util import assert_parity, gpu_gemm_dev, oracle_ref, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -95,3 +95,19 @@ def test_ready_calls_into_one_output_keep_stream_order(monkeypatch):
         Ce, S = oracle_ref(dict(ps[idx], A=A_bits))
         assert_parity(got.float().cpu().numpy().astype(np.float64), Ce, S, "bf16", f"call {idx} into a shared C")
     assert all(torch.equal(snaps[0], s) for s in snaps[1:])
+
+
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+@pytest.mark.parametrize("fmt,M,N,K", [("int4", 16, 1000, 512), ("int4", 4, 8192, 3072), ("nvfp4", 1, 264, 256),
+                                       ("mxfp4", 12, 520, 1024), ("int4", 16, 1004, 512)])
+def test_input_layout_pieces_same_bits(out, fmt, M, N, K, monkeypatch):
+    """The input-layout streaming kernel (wq_gemm at M <= 16) stores the same
+    bits in pieces as one output at a time, within the gate."""
+    p = synth.make_problem(fmt, M, N, K, seed=M + N + K)
+    monkeypatch.delenv("WQ_GEMV_SCALAR_STORE", raising=False)
+    C1 = gpu_gemm_dev(p, out)
+    monkeypatch.setenv("WQ_GEMV_SCALAR_STORE", "1")
+    C2 = gpu_gemm_dev(p, out)
+    assert torch.equal(C1, C2), f"{out} {fmt} {M}x{N}x{K}"
+    Ce, S = oracle_ref(p)
+    assert_parity(C1.float().cpu().numpy().astype(np.float64), Ce, S, out, f"input layout {out} {fmt} {M}x{N}x{K}")

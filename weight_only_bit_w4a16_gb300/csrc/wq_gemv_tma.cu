@@ -87,6 +87,7 @@ struct TmaGemvArgs {
     uint32_t SA;        // shared row stride of the activations (bytes)
     uint32_t w_off, a_off, r8_off, r4_off, bar_off, red_off;
     int inputs_ready;   // A may be read before the preceding kernel completes
+    int vec_store;      // plain output in 16-byte pieces: C 16-byte aligned, N a multiple of 8 (bf16) or 4 (fp32)
     Epilogue epi;
 };
 
@@ -223,6 +224,16 @@ __device__ __forceinline__ void warp_loop(uint32_t wp, uint32_t S8, uint32_t rp,
 // launches' CTAs fit on an SM; two tiles (M <= 16) hold 96 KB of activations
 // per CTA and never share an SM, so they take the registers to have all 16
 // rows of their activation loads in flight at once.
+// store_pieces as a call of its own: inlined, its registers pushed the
+// one-tile int4 instance (two 512-thread CTAs per SM, 64 registers) into
+// spilling
+template <int MP>
+__device__ __noinline__ void store_pieces_apart(const float* red, int ld, int Wk, int Mc, int outs_log2, int n0,
+                                                int n_end, int mz, int N, void* C, bool out_f32, int tid,
+                                                int nthreads) {
+    store_pieces<MP>(red, ld, Wk, Mc, outs_log2, n0, n_end, mz, N, C, out_f32, tid, nthreads);
+}
+
 template <int FMT, int NT, int MODE, bool EPI>
 __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_stream_kernel(const TmaGemvArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -411,6 +422,12 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_stream_kernel(const
     const bool gated = EPI && a.epi.gated;
     const int outs = gated ? rows >> 1 : rows;   // a power of two
     const int outs_log2 = 31 - __clz(outs);
+    if constexpr (!EPI) {
+        if (a.vec_store) {
+            store_pieces_apart<MP>(red, ld, Wk, Mc, outs_log2, n0, a.N, mz, a.N, a.C, a.out_f32, tid, blockDim.x);
+            return;
+        }
+    }
     for (int i = tid; i < Mc * outs; i += blockDim.x) {
         const int m = i >> outs_log2, o = i & (outs - 1);
         const int rl = gated ? (((o >> 3) << 4) | (o & 7)) : o;
@@ -624,6 +641,7 @@ int launch_gemv_tma(const void* A, const uint8_t* packed, const void* scales, co
     args.bar_off = plan.bar_off;
     args.red_off = plan.red_off;
     args.inputs_ready = inputs_ready ? 1 : 0;
+    args.vec_store = (reinterpret_cast<uintptr_t>(C) & 15) == 0 && N % (out_f32 ? 4 : 8) == 0 && !getenv("WQ_GEMV_SCALAR_STORE");
     args.epi = epi;
 
     cudaLaunchConfig_t cfg = {};

@@ -866,9 +866,10 @@ def run_e2e(args, w, A_by_M, weights, pool, dev, ws, pre_pool=None):
     # Every call is launched as a dependent chain (WQ_LAUNCH_OVERLAP): the
     # step's first call follows the copy of its activations through a full
     # dependency and overlaps only the previous step's last call; the staged
-    # kernel serves such chains.  Same GPU, 1000 pipelined steps: 1682 GB/s,
-    # against 1608 with the first call of each step launched plain, 1448 with
-    # every call's inputs declared ready, and 1046 with the later calls ready.
+    # kernel serves such chains.  Same GPU, 1000 pipelined steps: 1674 GB/s,
+    # against 1484 with every call's inputs declared ready, 1325 with the
+    # later two calls of a step ready, and 1079 with the first call plain and
+    # the later two ready.
     kw_later = {"overlap": args.launch != "plain"}
 
     def one(i, upload_weights=None):

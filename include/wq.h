@@ -236,18 +236,19 @@ size_t wq_workspace_bytes(int M, int N, int K, int format, int group);
  *            N and k past K hold code 0.
  *   records  from Nb * I * 1024, one record block per code block, in the
  *            same order:
- *              WQ_INT4   96 bytes.  Bytes 0..63: row r's two uint16
- *                        {bf16 scale, bf16 (128 + min(z, 128))} at
- *                        8 * (r & 7) + 4 * (r >> 3); bytes 64..95: row r's
- *                        bf16 (z - min(z, 128)) at 64 + 4 * (r & 7) +
- *                        2 * (r >> 3) (z the zero point; both subtrahends are
- *                        exact integers and (code - zero) is their exact
- *                        difference from 128 + code).  Rows past N: scale 0,
- *                        subtrahends 0x4300 (128) and 0.
+ *              WQ_INT4   48 bytes.  Bytes 0..31: row r's bf16 scale at
+ *                        4 * (r & 7) + 2 * (r >> 3); bytes 32..47: row r's
+ *                        uint8 zero point at 32 + 2 * (r & 7) + (r >> 3)
+ *                        (so rows r and r + 8 share one 4-byte and one
+ *                        2-byte load).  Rows past N: scale 0, zero 0.
  *              WQ_NVFP4  128 bytes; row r's 8 scale bytes (groups 8i ..
  *                        8i + 7) at 8r.  Groups past K and rows past N: 0.
  *              WQ_MXFP4  64 bytes; row r's 4 scale bytes (groups 4i ..
  *                        4i + 3) at 4r.  Groups past K and rows past N: 0.
+ *   flags    WQ_INT4 only: 16 bytes after the last record block; byte 0 is 1
+ *            when some zero point exceeds 128 (the kernels then subtract it
+ *            in two exact steps, 128 + min(z, 128) and z - min(z, 128)),
+ *            else 0; bytes 1..15 are 0.
  */
 
 /* Size in bytes of the prepacked buffer for this weight, 0 for a

@@ -17,21 +17,18 @@ restated here:
   order; int4 words hold ``k0 + 2s`` in nibble ``s`` and ``k0 + 2s + 1`` in
   nibble ``s + 4``.  Padding (rows past N, k past K): code 0.
 * records from ``Nb*I*1024``, one per code block:
-  int4 (group 128) 96 bytes: ``{bf16 scale, bf16(128 + min(z,128))}`` of row
-  r at ``8*(r&7) + 4*(r>>3)``, ``bf16(z - min(z,128))`` at
-  ``64 + 4*(r&7) + 2*(r>>3)``; padded rows ``{0, bf16(128)}`` and 0.
+  int4 (group 128) 48 bytes: row r's bf16 scale at ``4*(r&7) + 2*(r>>3)``,
+  its uint8 zero point at ``32 + 2*(r&7) + (r>>3)``; padded rows 0 and 0.
   NVFP4 128 bytes: row r's 8 scale bytes (groups ``8i..8i+7``) at ``8r``.
   MXFP4 64 bytes: row r's 4 scale bytes (groups ``4i..4i+3``) at ``4r``.
   Groups past K and padded rows: 0.
-
-The bf16 images of the subtrahends come from the oracle's own
-round-to-nearest-even (``round_bf16``), not from bit tricks.
+* int4 only, 16 bytes after the last record block: byte 0 is 1 when some
+  zero point exceeds 128, else 0; the rest 0.
 """
 from __future__ import annotations
 
 import numpy as np
 
-from . import round_bf16
 
 _INT4, _NVFP4, _MXFP4 = "int4", "nvfp4", "mxfp4"
 _WORD_ORDER = (0, 4, 1, 5, 2, 6, 3, 7)   # storage order of a half-row's words
@@ -44,12 +41,17 @@ def _fmt_name(fmt) -> str:
 
 def record_bytes(fmt) -> int:
     """Bytes of one record block."""
-    return {_INT4: 96, _NVFP4: 128, _MXFP4: 64}[_fmt_name(fmt)]
+    return {_INT4: 48, _NVFP4: 128, _MXFP4: 64}[_fmt_name(fmt)]
+
+
+def flag_bytes(fmt) -> int:
+    """Bytes after the record blocks (int4: the large-zero-point flag)."""
+    return 16 if _fmt_name(fmt) == _INT4 else 0
 
 
 def prepack_bytes(N: int, K: int, fmt) -> int:
     nb, nk = -(-N // 16), -(-K // 128)
-    return nb * nk * (1024 + record_bytes(fmt))
+    return nb * nk * (1024 + record_bytes(fmt)) + flag_bytes(fmt)
 
 
 def _codes(packed: np.ndarray, rows: int, cols: int) -> np.ndarray:
@@ -121,17 +123,15 @@ def prepack(packed, scales, zeros, fmt, group: int) -> np.ndarray:
                         s, z = int(s_bits[row, i]), int(z_all[row, i])
                     else:
                         s, z = 0, 0
-                    zc = min(z, 128)
-                    first = round_bf16(128.0 + zc)
-                    second = round_bf16(float(z - zc))
-                    p = at + 8 * (r & 7) + 4 * (r >> 3)
-                    out[p:p + 4] = [s & 0xFF, s >> 8, first & 0xFF, first >> 8]
-                    q = at + 64 + 4 * (r & 7) + 2 * (r >> 3)
-                    out[q:q + 2] = [second & 0xFF, second >> 8]
+                    p = at + 4 * (r & 7) + 2 * (r >> 3)
+                    out[p:p + 2] = [s & 0xFF, s >> 8]
+                    out[at + 32 + 2 * (r & 7) + (r >> 3)] = z
                 else:
                     per = 8 if fmt == _NVFP4 else 4
                     for g in range(per):
                         gi = per * i + g
                         if row < N and gi < ng:
                             out[at + per * r + g] = s_all[row, gi]
+    if fmt == _INT4 and N > 0 and bool((z_all > 128).any()):
+        out[rec0 + nb * nk * rb] = 1
     return out

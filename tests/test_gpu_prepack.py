@@ -106,7 +106,7 @@ def test_staged_cta_shapes(rb, wk, monkeypatch):
         nk = -(-K // 128)
         ipw = -(-nk // (1 << int(wk)))
         warps = int(rb) << int(wk)
-        rec = 96 if fmt == "int4" else 512
+        rec = 96 if fmt == "int4" else 512   # int4 reserves 96 B per block (48 used)
         # activation rows per CTA: 16 when they fit, else 8, 4, 2, 1
         fits = [256 + warps * ipw * (1024 + rec) + min(M, mr) * (nk * 256 + 64) + 128 <= 227 * 1024
                 for mr in (16, 8, 4, 2, 1)]
@@ -131,7 +131,7 @@ def _ring_smem(fmt, M, K, RB, Wk, P):
     Mc, MP = min(M, mrows), (16 if M > 8 else 8)
     ring_off = r128(8 * Wk * P)
     slot = r128(1024 * RB + 256 * Mc)
-    end = ring_off + Wk * P * slot + Wk * RB * ipw * (96 if fmt == "int4" else 512)
+    end = ring_off + Wk * P * slot + Wk * RB * ipw * (96 if fmt == "int4" else 512)   # int4: 96 reserved
     red = ring_off + Wk * MP * (RB * 16 + 4) * 4
     return max(end, red) + 128
 
@@ -172,6 +172,22 @@ def test_int4_zero_points_above_128(M, kernel):
     z[big] = rng.integers(129, 256, size=int(big.sum()), dtype=np.uint8)
     p["zeros"] = z
     check_pre(p, "fp32", what=f"{kernel} int4 big zeros M={M}", ready=ready_for(kernel))
+
+
+@pytest.mark.parametrize("M", [3, 16])
+def test_int4_zero_points_up_to_128(M, kernel):
+    """Zero points 0, 1, 127 and 128 only: the prepacked flag stays 0 and every
+    subtrahend is the one-step 128 + z (z = 128 carries into the exponent)."""
+    p = synth.make_problem("int4", M, 144, 1024, seed=M + 11)
+    rng = np.random.default_rng(M + 1)
+    p["zeros"] = rng.choice(np.array([0, 1, 127, 128], np.uint8), size=p["zeros"].shape)
+    pre = prepack_dev(p)
+    assert int(pre.buf[-16].item()) == 0
+    check_pre(p, "fp32", what=f"{kernel} int4 zeros <= 128 M={M}", ready=ready_for(kernel))
+    if M == 16:
+        C = run_tc(p)
+        Ce, S = oracle_ref(p)
+        assert_parity(C, Ce, S, "fp32", "tc int4 zeros <= 128")
 
 
 @pytest.mark.parametrize("M", [3, 16])

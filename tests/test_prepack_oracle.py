@@ -72,12 +72,13 @@ def test_hand_worked_positions(case):
 
 
 def test_sizes():
-    # Nb * I * (1024 + record block): 20 rows -> 2 blocks, K 256 -> 2 blocks
-    assert opk.prepack_bytes(20, 256, "int4") == 4 * (1024 + 96)
+    # Nb * I * (1024 + record block) (+ 16 flag bytes for int4): 20 rows -> 2
+    # blocks, K 256 -> 2 blocks
+    assert opk.prepack_bytes(20, 256, "int4") == 4 * (1024 + 48) + 16
     assert opk.prepack_bytes(20, 256, "nvfp4") == 4 * (1024 + 128)
     assert opk.prepack_bytes(20, 256, "mxfp4") == 4 * (1024 + 64)
-    assert opk.prepack_bytes(16, 128, "int4") == 1024 + 96
-    assert opk.prepack_bytes(8192, 3072, "int4") == 512 * 24 * 1120
+    assert opk.prepack_bytes(16, 128, "int4") == 1024 + 48 + 16
+    assert opk.prepack_bytes(8192, 3072, "int4") == 512 * 24 * 1072 + 16
 
 
 # -- an independent inverse ----------------------------------------------------
@@ -108,15 +109,13 @@ def unprepack(buf, N, K, fmt):
 
     rec = buf[nb * nk * 1024:]
     if fmt == "int4":
-        blocks = rec.reshape(nb, nk, 96)
-        first = blocks[:, :, :64].reshape(nb, nk, 8, 2, 4)                   # b i (r&7) (r>>3) bytes
-        first = first.transpose(0, 3, 2, 1, 4).reshape(nb * 16, nk, 4)        # row i bytes
-        second = blocks[:, :, 64:].reshape(nb, nk, 8, 2, 2).transpose(0, 3, 2, 1, 4).reshape(nb * 16, nk, 2)
-        s_bits = first[..., 0].astype(np.uint16) | (first[..., 1].astype(np.uint16) << 8)
-        z1 = first[..., 2].astype(np.uint16) | (first[..., 3].astype(np.uint16) << 8)
-        z2 = second[..., 0].astype(np.uint16) | (second[..., 1].astype(np.uint16) << 8)
-        zero = bf16_value(z1) - 128.0 + bf16_value(z2)
-        return packed, s_bits[:N], zero[:N], (s_bits[N:], bf16_value(z1[N:]), bf16_value(z2[N:]))
+        blocks = rec[:nb * nk * 48].reshape(nb, nk, 48)
+        sc = blocks[:, :, :32].reshape(nb, nk, 8, 2, 2)                       # b i (r&7) (r>>3) bytes
+        sc = sc.transpose(0, 3, 2, 1, 4).reshape(nb * 16, nk, 2)              # row i bytes
+        zp = blocks[:, :, 32:].reshape(nb, nk, 8, 2).transpose(0, 3, 2, 1).reshape(nb * 16, nk)
+        s_bits = sc[..., 0].astype(np.uint16) | (sc[..., 1].astype(np.uint16) << 8)
+        flags = rec[nb * nk * 48:]
+        return packed, s_bits[:N], zp[:N], (s_bits[N:], zp[N:], flags)
     per = 8 if fmt == "nvfp4" else 4
     blocks = rec.reshape(nb, nk, 16, per).transpose(0, 2, 1, 3).reshape(nb * 16, nk * per)
     ng = K // GROUP[fmt]
@@ -144,9 +143,10 @@ def test_round_trip(fmt, N, K):
     np.testing.assert_array_equal(p2, packed)
     if fmt == "int4":
         np.testing.assert_array_equal(s2, scales)
-        np.testing.assert_array_equal(z2, zeros.astype(np.float64))
-        s_pad, z1_pad, z2_pad = pad
-        assert not s_pad.any() and (z1_pad == 128.0).all() and not z2_pad.any()
+        np.testing.assert_array_equal(z2, zeros)
+        s_pad, z_pad, flags = pad
+        assert not s_pad.any() and not z_pad.any()
+        assert flags.size == 16 and int(flags[0]) == int((zeros > 128).any()) and not flags[1:].any()
     else:
         np.testing.assert_array_equal(s2, scales)
         assert not pad[0].any() and not pad[1].any()
@@ -159,9 +159,21 @@ def test_round_trip(fmt, N, K):
     assert nz_in == nz_out
 
 
+def test_large_zero_flag():
+    """The int4 flag byte is 1 exactly when some zero point exceeds 128
+    (128 itself is still one exact subtrahend)."""
+    packed = np.zeros((20, 128), np.uint8)
+    scales = np.zeros((20, 2), np.uint16)
+    for zmax, want in ((0, 0), (128, 0), (129, 1), (255, 1)):
+        zeros = np.zeros((20, 2), np.uint8)
+        zeros[19, 1] = zmax
+        buf = opk.prepack(packed, scales, zeros, "int4", 128)
+        assert int(buf[4 * (1024 + 48)]) == want, zmax
+
+
 def test_first_subtrahend_is_exact():
     # bf16(128 + min(z, 128)) and bf16(z - min(z, 128)) hold the zero point
-    # exactly for every uint8 z (the record's two subtrahends)
+    # exactly for every uint8 z (the decode's two subtrahends)
     for z in range(256):
         zc = min(z, 128)
         a, b = oracle.round_bf16(128.0 + zc), oracle.round_bf16(float(z - zc))

@@ -125,6 +125,21 @@ struct GroupKey {
 
 __device__ __forceinline__ uint32_t splat16(uint32_t h) { return (h & 0xFFFFu) * 0x10001u; }
 
+// int4 subtrahends from a prepacked record's zero-point pair zp = {z_r,
+// z_(r+8)} (bytes 0, 1): the bf16x2 splat of 128 + z for row r (zsub_lo) and
+// row r + 8 (zsub_hi).  0x43 over the byte z is 128 + z exactly for z <= 127,
+// and z = 128 carries into the exponent: 0x4380 = 256.  Larger zero points
+// take zsub_two.
+__device__ __forceinline__ uint32_t zsub_lo(uint32_t zp) { return prmt(zp, 0x43u, 0x4040u); }
+__device__ __forceinline__ uint32_t zsub_hi(uint32_t zp) { return prmt(zp, 0x43u, 0x4141u); }
+// Any uint8 zero point z: the two exact subtrahends 128 + min(z, 128) and
+// z - min(z, 128), as bf16x2 splats.
+__device__ __forceinline__ void zsub_two(uint32_t z, uint32_t& first, uint32_t& second) {
+    const uint32_t zc = min(z, 128u);
+    first = splat16(0x4300u + zc);
+    second = splat16(__bfloat16_as_ushort(__float2bfloat16_rn((float)(z - zc))));
+}
+
 // bf16 bits of |e4m3(b)| * 2^112 (exact: at most 4 significant bits, range
 // 2^103 .. 1.75*2^120).  NaN (S.1111.111) gives a NaN multiplier; the sign
 // bit is ignored (the weight uses |scale|).

@@ -19,9 +19,9 @@
 // then arrive (without a count increment) on the slot's mbarrier, an arrival
 // that happens once their copies have landed; a phase of 32 arrivals
 // therefore means the whole slot is in shared memory.  The warp refills the
-// slot with step t + P once step t's MMAs are done.  The int4 decode records
-// of the warp's range (96 bytes per block, already in the form the loop
-// reads) are copied once, ahead of step 0.  The small CTA footprint lets the
+// slot with step t + P once step t's MMAs are done.  The int4 records of the
+// warp's range (48 bytes per block: scales and zero points) are copied once,
+// ahead of step 0.  The small CTA footprint lets the
 // CTAs of several consecutive calls share an SM, so that one call's weights
 // stream while another's decode runs.
 //
@@ -34,7 +34,7 @@
 //   bars  [Wk][P] u64 at 0                     slot landed (32 arrivals)
 //   ring  [Wk][P][slot_bytes] at ring_off      RB code blocks, then the
 //                                              activation rows (256 B, swizzled)
-//   recs  [Wk][RB][ipw][96]  int4 at rec_off   the copied record blocks
+//   recs  [Wk][RB][ipw][48]  int4 at rec_off   the copied record blocks
 //         [Wk][RB][ipw][512] fp4               decoded multipliers, per lane
 //   red   [Wk][MP][RB*16 + 4] f32 at ring_off  partial sums (aliases ring/recs)
 #include <cstdio>
@@ -236,17 +236,18 @@ __device__ __forceinline__ void step_int4_group(uint32_t wp0, uint32_t rec0, uin
         block_words(wp0 + 1024u * q, qa, qb);
         wa[q][0] = qa.x; wa[q][1] = qa.y; wa[q][2] = qa.z; wa[q][3] = qa.w;
         wb[q][0] = qb.x; wb[q][1] = qb.y; wb[q][2] = qb.z; wb[q][3] = qb.w;
+        // rows r and r + 8: bf16 scales at 4r, zero points at 32 + 2r
         const uint32_t rec = rec0 + rec_stride * q;
-        const uint2 rr = lds64(rec + 8u * r);
-        zzA[q] = prmt(rr.x, rr.x, 0x3232u);
-        zzB[q] = prmt(rr.y, rr.y, 0x3232u);
-        sa[q] = __uint_as_float(rr.x << 16);
-        sb[q] = __uint_as_float(rr.y << 16);
-        zzA2[q] = zzB2[q] = 0;
+        const uint32_t sp = lds32(rec + 4u * r), zp = lds16(rec + 32u + 2u * r);
+        sa[q] = __uint_as_float(sp << 16);
+        sb[q] = __uint_as_float(sp & 0xFFFF0000u);
         if constexpr (TWO) {
-            const uint32_t z2 = lds32(rec + 64u + 4u * r);
-            zzA2[q] = splat16(z2);
-            zzB2[q] = splat16(z2 >> 16);
+            zsub_two(zp & 0xFFu, zzA[q], zzA2[q]);
+            zsub_two(zp >> 8, zzB[q], zzB2[q]);
+        } else {
+            zzA[q] = zsub_lo(zp);
+            zzB[q] = zsub_hi(zp);
+            zzA2[q] = zzB2[q] = 0;
         }
     }
     // one MMA chain per tile and row block: the QI row blocks' chains are
@@ -332,7 +333,7 @@ template <int FMT, int NT, int RB, bool TWO>
 __device__ __forceinline__ bool run_range(const Ring<RB, NT>& ring, uint32_t lane_w, const uint32_t (&aoffE)[NT],
                                           const uint32_t (&aoffO)[NT], uint32_t rslice, uint32_t rlane, int ipw,
                                           float (&acc)[RB][NT][4]) {
-    constexpr uint32_t kRec = FMT == kINT4 ? 96 : 512;
+    constexpr uint32_t kRec = FMT == kINT4 ? 48 : 512;
     int slot = 0;
     uint32_t ph = 0;
     for (int i = 0; i < ring.nit; ++i) {
@@ -384,7 +385,7 @@ __global__ void __launch_bounds__(256, 2) gemv_pre_kernel(const PreArgs a) {
     const uint32_t sbase = (smem_u32(smem_raw) + 127u) & ~127u;
     uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
     constexpr bool kInt4 = FMT == kINT4;
-    constexpr uint32_t kRec = kInt4 ? 96 : 512;   // shared record bytes per row block and k-block
+    constexpr uint32_t kRec = kInt4 ? 48 : 512;   // shared record bytes per row block and k-block
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Wk = blockDim.x >> 5;
     const int r = lane >> 2, c = lane & 3;
@@ -422,6 +423,9 @@ __global__ void __launch_bounds__(256, 2) gemv_pre_kernel(const PreArgs a) {
     ring.P = a.P;
     ring.lane = lane;
     const int npro = min(a.P, nit);
+    // int4: the prepacked weight's flag (a zero point above 128 anywhere),
+    // read now and needed once step 0 has landed
+    const uint32_t large_zero = kInt4 ? ldg_u32(a.recs + (size_t)a.Nb * a.I * 48) : 0u;
 
     // with the inputs declared ready nothing waits on the preceding kernel
     // before the stores, so the next call may be scheduled at once
@@ -435,9 +439,9 @@ __global__ void __launch_bounds__(256, 2) gemv_pre_kernel(const PreArgs a) {
     if (nit > 0) {
         if constexpr (kInt4) {
             for (int q = 0; q < nb; ++q)
-                for (int u = lane; u < nit * 6; u += 32)
-                    cp_async16(rslice + (uint32_t)(q * a.ipw) * 96u + 16u * u,
-                               a.recs + ((size_t)(bs + q) * a.I + it0) * 96 + 16 * u);
+                for (int u = lane; u < nit * 3; u += 32)
+                    cp_async16(rslice + (uint32_t)(q * a.ipw) * 48u + 16u * u,
+                               a.recs + ((size_t)(bs + q) * a.I + it0) * 48 + 16 * u);
         }
         for (int t = 0; t < npro; ++t) ring.issue_codes(t, t);
     }
@@ -508,15 +512,7 @@ __global__ void __launch_bounds__(256, 2) gemv_pre_kernel(const PreArgs a) {
         ok = ring.wait(0, 0u, dummy);   // step 0 (and the int4 records)
         if (!ok) ring.drain(1, npro);
     }
-    if constexpr (kInt4) {
-        // a zero point above 128 anywhere in the range: second subtrahends
-        bool t2 = false;
-        if (ok)
-            for (int q = 0; q < nb; ++q)
-                for (int u = lane; u < nit * 16; u += 32)
-                    t2 |= lds16(rslice + (uint32_t)(q * a.ipw + (u >> 4)) * 96u + 64u + 2u * (u & 15)) != 0;
-        two = __any_sync(0xffffffffu, t2);
-    }
+    if constexpr (kInt4) two = (large_zero & 0xFFu) != 0;   // some zero point above 128: two subtrahends
     if (ok && nit > 0) {
         // activation rows past Mc are not copied: those lanes read row 0 or 1
         // (keeping the row parity of a copied neighbour); their outputs are
@@ -631,6 +627,11 @@ Plan layout(int RB, int Wk, int P, int Mc, int I, int fmt, int MP) {
     p.ring_off = round128((size_t)8 * Wk * p.P);
     p.slot_bytes = round128((size_t)1024 * RB + (size_t)kAStride * Mc);
     p.rec_off = p.ring_off + (uint32_t)(Wk * p.P) * p.slot_bytes;
+    // int4 records take 48 bytes per block, but 96 are reserved: with the
+    // smaller CTAs more calls overlap on an SM, and a chain of calls of
+    // mixed M then collapses in some orders (same GPU: M = 1, 4, 16 in turn
+    // 9.5 -> 22.5 us per step), later calls taking the issue slots of the
+    // oldest one, whose completion every later store waits for
     const size_t end = p.rec_off + (size_t)Wk * RB * p.ipw * (fmt == kINT4 ? 96 : 512);
     const size_t red = p.ring_off + (size_t)Wk * MP * (RB * 16 + 4) * sizeof(float);
     p.smem = (end > red ? end : red) + 128;   // + base alignment slack

@@ -11,8 +11,8 @@
 // activations its N = 8 operand; int4 g128 runs the MMAs on the exact
 // integers (code - zero) and scales the fp32 partial sums per iteration.
 //   - per warp, its codes are ONE bulk copy (nit contiguous 1024-byte
-//     blocks) and, for int4, its decode records a second one (nit x 96
-//     bytes, already in the form the loop reads);
+//     blocks) and, for int4, its records a second one (nit x 48 bytes of
+//     scales and zero points);
 //   - the activations need no permutation (a lane's four words of a block
 //     are the natural k units c + 4j), so after the dependency wait the first
 //     warp of each K range copies them with one bulk copy per row and the
@@ -22,7 +22,7 @@
 //   bars  [warps] u64 at 0, [Wk] u64 at 128   codes / activations landed
 //   W     [warps][ipw][1024]                  the warps' code blocks
 //   A     [Mc][SA]                            activation rows, natural order
-//   R     [warps][ipw][96]  int4              the copied record blocks
+//   R     [warps][ipw][48]  int4              the copied record blocks
 //         [warps][ipw][512] fp4               decoded multipliers, per lane
 //   red   [Wk][MP][rows + 4] f32 at 256       partial sums (aliases W, A, R)
 #include <cstdio>
@@ -96,9 +96,9 @@ __device__ __forceinline__ void block_words(uint32_t wp, uint4& qa, uint4& qb) {
     qb = make_uint4(b0.x, b0.y, b1.x, b1.y);
 }
 
-// int4 g128 loop.  rp: the lane's record pair {row r, row r + 8} (4 bytes
-// each: bf16 scale | bf16 (128 + min(z, 128)) << 16); rq: the pair of second
-// subtrahends (2 bytes each, read only when some zero point exceeds 128).
+// int4 g128 loop.  rp: the lane's scale pair {row r, row r + 8} (bf16 each);
+// rq: its zero-point pair (a byte each).  TWO: some zero point exceeds 128,
+// so each is subtracted in two exact steps.
 template <int NT, bool TWO>
 __device__ __forceinline__ void loop_int4(uint32_t wp, uint32_t rp, uint32_t rq, uint32_t (&ap)[NT], int nit,
                                           float (&acc)[NT][4]) {
@@ -107,18 +107,20 @@ __device__ __forceinline__ void loop_int4(uint32_t wp, uint32_t rp, uint32_t rq,
     for (int i = 0; i < nit; ++i) {
         uint4 qa, qb;
         block_words(wp, qa, qb);
-        const uint2 rr = lds64(rp);
-        uint32_t zA2 = 0, zB2 = 0;
+        const uint32_t sp = lds32(rp), zp = lds16(rq);
+        uint32_t zA, zB, zA2 = 0, zB2 = 0;
         if constexpr (TWO) {
-            const uint32_t q = lds32(rq);
-            zA2 = splat16(q);
-            zB2 = splat16(q >> 16);
+            zsub_two(zp & 0xFFu, zA, zA2);
+            zsub_two(zp >> 8, zB, zB2);
+        } else {
+            zA = zsub_lo(zp);
+            zB = zsub_hi(zp);
         }
-        it_int4<NT, TWO>(qa, qb, ap, acc, prmt(rr.x, rr.x, 0x3232u), zA2, prmt(rr.y, rr.y, 0x3232u), zB2,
-                         __uint_as_float(rr.x << 16), __uint_as_float(rr.y << 16));
+        it_int4<NT, TWO>(qa, qb, ap, acc, zA, zA2, zB, zB2, __uint_as_float(sp << 16),
+                         __uint_as_float(sp & 0xFFFF0000u));
         wp += 1024;
-        rp += 96;
-        rq += 96;
+        rp += 48;
+        rq += 48;
 #pragma unroll
         for (int t = 0; t < NT; ++t) ap[t] += 256;
     }
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_staged_kernel(const
     const uint32_t sbase = (smem_u32(smem_raw) + 127u) & ~127u;
     uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
     constexpr bool kInt4 = FMT == kINT4;
-    constexpr uint32_t kRec = kInt4 ? 96 : 512;   // shared record bytes per warp and block
+    constexpr uint32_t kRec = kInt4 ? 48 : 512;   // shared record bytes per warp and block
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = lane >> 2, c = lane & 3;
     const int Wk = 1 << a.wk_log2;
@@ -197,6 +199,8 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_staged_kernel(const
     const uint32_t wslice = sbase + a.w_off + (uint32_t)(warp * a.ipw) * 1024u;
     const uint32_t rslice = sbase + a.r_off + (uint32_t)(warp * a.ipw) * kRec;
     const size_t blk0 = (size_t)b * a.I + it0;
+    // int4: the prepacked weight's flag (a zero point above 128 anywhere)
+    const uint32_t large_zero = kInt4 ? ldg_u32(a.recs + (size_t)a.Nb * a.I * 48) : 0u;
 
     if (tid == 0) {
         for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mbar_init(sbase + 8 * w, 1);
@@ -207,10 +211,10 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_staged_kernel(const
 
     // ---- 1. this warp's code blocks (and int4 record blocks), one copy each
     if (lane == 0) {
-        mbar_arrive_expect_tx(bar, (uint32_t)nit * (1024u + (kInt4 ? 96u : 0u)));
+        mbar_arrive_expect_tx(bar, (uint32_t)nit * (1024u + (kInt4 ? 48u : 0u)));
         if (nit > 0) {
             bulk_copy_g2s(wslice, a.codes + blk0 * 1024, (uint32_t)nit * 1024u, bar);
-            if constexpr (kInt4) bulk_copy_g2s(rslice, a.recs + blk0 * 96, (uint32_t)nit * 96u, bar);
+            if constexpr (kInt4) bulk_copy_g2s(rslice, a.recs + blk0 * 48, (uint32_t)nit * 48u, bar);
         }
     }
 
@@ -286,13 +290,7 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_staged_kernel(const
         for (int e = 0; e < 4; ++e) acc[t][e] = 0.f;
     bool ok = mbar_wait_timeout(bar, 0, kWaitNs);
     ok = mbar_wait_timeout(abar, 0, kWaitNs) && ok;
-    if constexpr (kInt4) {
-        // a zero point above 128 anywhere in the slice: second subtrahends
-        bool t2 = false;
-        if (ok)
-            for (int q = lane; q < nit * 16; q += 32) t2 |= lds16(rslice + (q >> 4) * 96 + 64 + 2 * (q & 15)) != 0;
-        two = __any_sync(0xffffffffu, t2);
-    }
+    if constexpr (kInt4) two = (large_zero & 0xFFu) != 0;   // some zero point above 128: two subtrahends
     if (ok && nit > 0) {
         // activation rows past Mc are not staged: those lanes read row 0 or 1
         // (keeping the row parity of a staged neighbour)
@@ -310,7 +308,7 @@ __global__ void __launch_bounds__(512, NT == 1 ? 2 : 1) gemv_staged_kernel(const
 #pragma unroll
         for (int t = 0; t < NT; ++t) asm volatile("" : "+r"(ap[t])::"memory");
         if constexpr (kInt4) {
-            const uint32_t rp = rslice + 8u * r, rq = rslice + 64u + 4u * r;
+            const uint32_t rp = rslice + 4u * r, rq = rslice + 32u + 2u * r;
             if (two) loop_int4<NT, true>(wp, rp, rq, ap, nit, acc);
             else loop_int4<NT, false>(wp, rp, rq, ap, nit, acc);
         } else {
@@ -406,6 +404,9 @@ Plan layout(int rb, int wk_log2, int Mc, int I, int fmt, int MP) {
     p.SA = (uint32_t)I * 256 + 64;   // 64 (mod 128): row parities in opposite bank halves
     off += (size_t)Mc * p.SA;
     p.r_off = (uint32_t)off;
+    // int4 records take 48 bytes per block; 96 are reserved, the footprint
+    // of the format before (its plans and the overlap between calls that
+    // the CTA size sets were measured with it)
     off += warps * p.ipw * (fmt == kINT4 ? 96 : 512);
     p.red_off = kBarBytes;           // aliases W, A and R once every warp is done
     const size_t red = ((size_t)1 << wk_log2) * MP * (rows + 4) * sizeof(float);

@@ -17,8 +17,11 @@
 //     the activations are copied as they are (no permutation);
 //   - int4 words hold the pairs (k0 + 2s, k0 + 2s + 1) in nibbles (s, s + 4),
 //     so the one-mask decode gives bf16 pairs of consecutive k;
-//   - the int4 records hold the two exact subtrahends of the decode, ready
-//     for the loop, next to the scale.
+//   - the int4 records hold each row's bf16 scale and uint8 zero point, rows
+//     r and r + 8 side by side (one 4-byte and one 2-byte load per lane);
+//     the loop forms the subtrahend 128 + z from the zero byte with one
+//     byte permute, and a flag after the records says whether any zero
+//     point exceeds 128 (then it is subtracted in two exact steps).
 // A half block (16 rows x 64 k, 512 bytes) has the byte placement of a tile
 // of 32-byte rows under the 32-byte swizzle (16-byte chunks exchanged on bit
 // 2 of the row), the placement a tensor-map copy of 64 k of the natural rows
@@ -33,8 +36,10 @@ namespace {
 constexpr int kBlockBytes = 1024;
 
 __host__ __device__ constexpr int record_block_bytes(int fmt) {
-    return fmt == kINT4 ? 96 : (fmt == kNVFP4 ? 128 : 64);
+    return fmt == kINT4 ? 48 : (fmt == kNVFP4 ? 128 : 64);
 }
+// int4: the flag block after the record blocks (byte 0: a zero point > 128)
+constexpr int kFlagBytes = 16;
 
 // int4: nibble q of the input word holds k0 + q; the output word holds
 // k0 + 2s in nibble s and k0 + 2s + 1 in nibble s + 4
@@ -91,13 +96,13 @@ __global__ void __launch_bounds__(256) prepack_kernel(const uint8_t* __restrict_
             s = static_cast<const uint16_t*>(scales)[gi];
             z = zeros[gi];
         }
-        const uint32_t zc = min(z, 128u);
-        // 128 + zc is exact in bf16 (8 significant bits): 0x4300 is 128.0 and
-        // zc lands in the mantissa, zc = 128 carrying into the exponent
-        const uint32_t first = 0x4300u + zc;
-        const uint32_t second = __bfloat16_as_ushort(__float2bfloat16_rn((float)(z - zc)));
-        *reinterpret_cast<uint32_t*>(rec + 8 * (r & 7) + 4 * (r >> 3)) = s | (first << 16);
-        *reinterpret_cast<uint16_t*>(rec + 64 + 4 * (r & 7) + 2 * (r >> 3)) = (uint16_t)second;
+        *reinterpret_cast<uint16_t*>(rec + 4 * (r & 7) + 2 * (r >> 3)) = (uint16_t)s;
+        rec[32 + 2 * (r & 7) + (r >> 3)] = (uint8_t)z;
+        if (z > 128u) {   // the flag block follows the last record block (zeroed before this kernel)
+            const size_t at = (size_t)Nb * I * (kBlockBytes + record_block_bytes(kINT4));
+            uint32_t* flag = reinterpret_cast<uint32_t*>(out + at);
+            atomicOr(flag, 1u);
+        }
     } else {
         constexpr int per = FMT == kNVFP4 ? 8 : 4;   // groups of a row in a 128-k block
         const int ng = K / (FMT == kNVFP4 ? 16 : 32);
@@ -114,7 +119,7 @@ __global__ void __launch_bounds__(256) prepack_kernel(const uint8_t* __restrict_
 
 size_t prepack_bytes(int N, int K, int fmt) {
     const size_t nb = (size_t)(N + 15) / 16, nk = (size_t)(K + 127) / 128;
-    return nb * nk * (size_t)(kBlockBytes + record_block_bytes(fmt));
+    return nb * nk * (size_t)(kBlockBytes + record_block_bytes(fmt)) + (fmt == kINT4 ? kFlagBytes : 0);
 }
 
 int launch_prepack(const uint8_t* packed, const void* scales, const uint8_t* zeros, void* out, int N, int K,
@@ -123,6 +128,10 @@ int launch_prepack(const uint8_t* packed, const void* scales, const uint8_t* zer
     const long long blocks = ((long long)Nb * I + 7) / 8;
     if (blocks > 0x7FFFFFFFLL) return WQ_ERR_UNSUPPORTED;
     uint8_t* o = static_cast<uint8_t*>(out);
+    if (fmt == kINT4 &&
+        cudaMemsetAsync(o + (size_t)Nb * I * (kBlockBytes + record_block_bytes(kINT4)), 0, kFlagBytes, stream) !=
+            cudaSuccess)
+        return WQ_ERR_CUDA;
     if (fmt == kINT4)
         prepack_kernel<kINT4><<<(unsigned)blocks, 256, 0, stream>>>(packed, scales, zeros, o, N, K, Nb, I);
     else if (fmt == kNVFP4)

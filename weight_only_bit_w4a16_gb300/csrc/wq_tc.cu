@@ -236,7 +236,9 @@ __device__ __forceinline__ void decode_row(const uint4& c0, const uint4& c1, con
 // (n / 16, ks / 2), row n % 16, half ks % 2):
 //   nvfp4: the 4 bytes of groups 4ks..4ks+3 (the row's 8 bytes at 8 r)
 //   mxfp4: the 2 bytes of groups 2ks, 2ks+1 (the row's 4 bytes at 4 r)
-//   int4 : {bf16 scale | bf16 (128 + min(z, 128)) << 16}, bf16 (z - min(z, 128))
+//   int4 : the row's bf16 scale (at 4 (r & 7) + 2 (r >> 3)) and zero point
+//          (at 32 + 2 (r & 7) + (r >> 3)), returned as the input layout's
+//          {bf16 scale | bf16 (128 + min(z, 128)) << 16}, bf16 (z - min(z, 128))
 template <int FMT>
 __device__ __forceinline__ uint2 tc_raw_pre(const TcArgs& a, int n, int ks) {
     const size_t blk = (size_t)(n >> 4) * a.kblocks + (ks >> 1);
@@ -249,9 +251,12 @@ __device__ __forceinline__ uint2 tc_raw_pre(const TcArgs& a, int n, int ks) {
         raw.x = ldg_u16(a.scales + blk * 64 + 4 * r + 2 * h);
         raw.y = 0;
     } else {
-        const uint8_t* rec = a.scales + blk * 96;
-        raw.x = ldg_u32(rec + 8 * (r & 7) + 4 * (r >> 3));
-        raw.y = ldg_u16(rec + 64 + 4 * (r & 7) + 2 * (r >> 3));
+        const uint8_t* rec = a.scales + blk * 48;
+        const uint32_t s = ldg_u16(rec + 4 * (r & 7) + 2 * (r >> 3));
+        const uint32_t z = __ldg(rec + 32 + 2 * (r & 7) + (r >> 3));
+        const uint32_t zc = min(z, 128u);
+        raw.x = s | ((0x4300u + zc) << 16);   // 128 + zc, exact in bf16
+        raw.y = z > 128u ? (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn((float)(z - zc))) : 0u;
     }
     return raw;
 }
